@@ -1,0 +1,259 @@
+"""Paged ragged attention and KV handoff for NVIDIA GB300 (sm_103a).
+
+A thin Python binding over the C ABI in ``include/pd.h`` (``libpd.so``, built
+in-tree by ``decode_ragged_paged_gb300.build``). The functions carry the C
+names and only marshal arguments: torch tensors give device pointers, shapes
+and the current CUDA stream; every step of the computation runs in the
+library's CUDA kernels. There is no CPU path: if ``libpd.so`` is missing or a
+call fails, an exception is raised.
+
+Tensor layouts (see ``include/pd.h``):
+    q, o            [total_qo][Hq][D]        fp32 or bf16
+    k_pool, v_pool  [num_pages][Hkv][P][D]   HND pages
+    qo_indptr       int32 [B+1]; kv_len int32 [B]; page_indptr int32 [B+1];
+    page_indices    int32 [nnz]
+    lse             fp32 [total_qo][Hq], natural log
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpd.so")
+
+PD_OK, PD_ERR_INVALID_ARG, PD_ERR_UNSUPPORTED, PD_ERR_WORKSPACE, PD_ERR_CUDA = 0, -1, -2, -3, -4
+PD_F32, PD_BF16 = 0, 1
+PD_LAYOUT_HND = 0
+PD_KIND_DECODE, PD_KIND_PREFILL, PD_KIND_MIXED = 0, 1, 2
+DEVICE_STATUS = {0: "ok", 1: "bad indptr", 2: "bad length", 3: "bad page table", 4: "not a decode",
+                 5: "timeout", 6: "bad offset"}
+
+# Every symbol include/pd.h declares.
+EXPORTS = ("pd_attn_workspace_size", "pd_attn_decode", "pd_attn_prefill", "pd_attn_mixed",
+           "pd_kv_append", "pd_kv_pack", "pd_kv_unpack", "pd_status_string",
+           "pd_device_status_string", "pd_version")
+
+
+class PdError(RuntimeError):
+    pass
+
+
+class AttnDesc(ctypes.Structure):
+    _fields_ = [("num_qo_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("o_dtype", ctypes.c_int32),
+                ("layout", ctypes.c_int32), ("causal", ctypes.c_int32), ("sm_scale", ctypes.c_float)]
+
+
+class Batch(ctypes.Structure):
+    _fields_ = [("batch_size", ctypes.c_int32), ("qo_indptr", ctypes.c_void_p),
+                ("kv_len", ctypes.c_void_p), ("page_indptr", ctypes.c_void_p),
+                ("page_indices", ctypes.c_void_p), ("num_pages", ctypes.c_int32),
+                ("total_qo", ctypes.c_int32), ("max_qo_len", ctypes.c_int32),
+                ("max_kv_len", ctypes.c_int32)]
+
+
+class KvDesc(ctypes.Structure):
+    _fields_ = [("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("dtype", ctypes.c_int32), ("layout", ctypes.c_int32),
+                ("num_layers", ctypes.c_int32), ("layer_stride_bytes", ctypes.c_int64)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libpd.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise PdError(f"{path} not found: build it with `python -m decode_ragged_paged_gb300.build`")
+            lib = ctypes.CDLL(path)
+            P, S, I32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+            attn = [ctypes.POINTER(AttnDesc), ctypes.POINTER(Batch), P, P, P, P, P, P, S, P, P]
+            for name in ("pd_attn_decode", "pd_attn_prefill", "pd_attn_mixed"):
+                getattr(lib, name).argtypes = attn
+                getattr(lib, name).restype = ctypes.c_int
+            lib.pd_attn_workspace_size.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(Batch), I32]
+            lib.pd_attn_workspace_size.restype = S
+            lib.pd_kv_append.argtypes = [ctypes.POINTER(KvDesc), ctypes.POINTER(Batch), P, P, P, P, P, P]
+            lib.pd_kv_pack.argtypes = [ctypes.POINTER(KvDesc), ctypes.POINTER(Batch), P, P, P, S, P, P, P]
+            lib.pd_kv_unpack.argtypes = [ctypes.POINTER(KvDesc), ctypes.POINTER(Batch), P, S, P, P, P, P, P]
+            for name in ("pd_kv_append", "pd_kv_pack", "pd_kv_unpack"):
+                getattr(lib, name).restype = ctypes.c_int
+            lib.pd_status_string.argtypes = [I32]
+            lib.pd_status_string.restype = ctypes.c_char_p
+            lib.pd_device_status_string.argtypes = [I32]
+            lib.pd_device_status_string.restype = ctypes.c_char_p
+            lib.pd_version.restype = I32
+            _lib = lib
+        return _lib
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != PD_OK:
+        msg = load_library().pd_status_string(rc).decode()
+        raise PdError(f"{what} failed: {msg} ({rc})")
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return PD_F32
+    if dt == torch.bfloat16:
+        return PD_BF16
+    raise PdError(f"unsupported dtype {dt}")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _i32(t, name):
+    if t is None:
+        return None
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise PdError(f"{name} must be a contiguous int32 CUDA tensor")
+    return t
+
+
+def make_attn_desc(q, k_pool, *, causal=True, sm_scale=None, o_dtype=None) -> AttnDesc:
+    num_pages, hkv, page, d = k_pool.shape
+    return AttnDesc(q.shape[1], hkv, d, page, _dtype_code(q.dtype),
+                    _dtype_code(o_dtype if o_dtype is not None else q.dtype), PD_LAYOUT_HND,
+                    int(bool(causal)), float(sm_scale) if sm_scale else 0.0)
+
+
+def make_batch(kv_len, page_indptr, page_indices, num_pages, *, qo_indptr=None, total_qo=0,
+               max_qo_len=1, max_kv_len=None) -> Batch:
+    _i32(kv_len, "kv_len"), _i32(page_indptr, "page_indptr"), _i32(page_indices, "page_indices")
+    _i32(qo_indptr, "qo_indptr")
+    if max_kv_len is None:  # convenience path: reads the lengths back (synchronises)
+        max_kv_len = int(kv_len.max().item()) if kv_len.numel() else 0
+    return Batch(kv_len.numel(), _ptr(qo_indptr), _ptr(kv_len), _ptr(page_indptr), _ptr(page_indices),
+                 int(num_pages), int(total_qo), int(max_qo_len), int(max_kv_len))
+
+
+def pd_attn_workspace_size(desc: AttnDesc, batch: Batch, kind: int) -> int:
+    return int(load_library().pd_attn_workspace_size(ctypes.byref(desc), ctypes.byref(batch), kind))
+
+
+def _attn(name, kind, q, k_pool, v_pool, kv_len, page_indptr, page_indices, qo_indptr, *, causal,
+          sm_scale, max_qo_len, max_kv_len, o, lse, o_dtype, workspace, dev_status, stream):
+    lib = load_library()
+    for t, n in ((q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool")):
+        if not t.is_cuda or not t.is_contiguous():
+            raise PdError(f"{n} must be a contiguous CUDA tensor")
+    desc = make_attn_desc(q, k_pool, causal=causal, sm_scale=sm_scale, o_dtype=o_dtype)
+    batch = make_batch(kv_len, page_indptr, page_indices, k_pool.shape[0], qo_indptr=qo_indptr,
+                       total_qo=q.shape[0], max_qo_len=max_qo_len, max_kv_len=max_kv_len)
+    if o is None:
+        o = torch.empty(q.shape, dtype=o_dtype if o_dtype is not None else q.dtype, device=q.device)
+    if lse is True:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    elif lse is False:
+        lse = None
+    need = pd_attn_workspace_size(desc, batch, kind)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = getattr(lib, name)(ctypes.byref(desc), ctypes.byref(batch), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                            _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                            _stream(stream))
+    _check(rc, name)
+    return o, lse
+
+
+def pd_attn_decode(q, k_pool, v_pool, kv_len, page_indptr, page_indices, qo_indptr=None, *, sm_scale=None,
+                   max_kv_len=None, o=None, lse=True, o_dtype=None, workspace=None, dev_status=None,
+                   stream=None):
+    """Decode attention: one query row per request. Returns (o, lse)."""
+    return _attn("pd_attn_decode", PD_KIND_DECODE, q, k_pool, v_pool, kv_len, page_indptr, page_indices,
+                 qo_indptr, causal=True, sm_scale=sm_scale, max_qo_len=1, max_kv_len=max_kv_len, o=o,
+                 lse=lse, o_dtype=o_dtype, workspace=workspace, dev_status=dev_status, stream=stream)
+
+
+def pd_attn_prefill(q, k_pool, v_pool, kv_len, page_indptr, page_indices, qo_indptr, *, causal=True,
+                    sm_scale=None, max_qo_len=None, max_kv_len=None, o=None, lse=True, o_dtype=None,
+                    workspace=None, dev_status=None, stream=None):
+    """Prefill attention over ragged query rows (qo_len <= kv_len). Returns (o, lse)."""
+    if max_qo_len is None:
+        max_qo_len = int((qo_indptr[1:] - qo_indptr[:-1]).max().item()) if qo_indptr.numel() > 1 else 0
+    return _attn("pd_attn_prefill", PD_KIND_PREFILL, q, k_pool, v_pool, kv_len, page_indptr, page_indices,
+                 qo_indptr, causal=causal, sm_scale=sm_scale, max_qo_len=max_qo_len, max_kv_len=max_kv_len,
+                 o=o, lse=lse, o_dtype=o_dtype, workspace=workspace, dev_status=dev_status, stream=stream)
+
+
+def pd_attn_mixed(q, k_pool, v_pool, kv_len, page_indptr, page_indices, qo_indptr, *, causal=True,
+                  sm_scale=None, max_qo_len=None, max_kv_len=None, o=None, lse=True, o_dtype=None,
+                  workspace=None, dev_status=None, stream=None):
+    """Mixed prefill + decode batch in one launch. Returns (o, lse)."""
+    if max_qo_len is None:
+        max_qo_len = int((qo_indptr[1:] - qo_indptr[:-1]).max().item()) if qo_indptr.numel() > 1 else 0
+    return _attn("pd_attn_mixed", PD_KIND_MIXED, q, k_pool, v_pool, kv_len, page_indptr, page_indices,
+                 qo_indptr, causal=causal, sm_scale=sm_scale, max_qo_len=max_qo_len, max_kv_len=max_kv_len,
+                 o=o, lse=lse, o_dtype=o_dtype, workspace=workspace, dev_status=dev_status, stream=stream)
+
+
+def _kv_desc(pool, num_layers=1, layer_stride_bytes=0) -> KvDesc:
+    """pool: [num_pages][Hkv][P][D] or [L][num_pages][Hkv][P][D]."""
+    shape = pool.shape[-4:]
+    return KvDesc(shape[1], shape[3], shape[2], _dtype_code(pool.dtype), PD_LAYOUT_HND, int(num_layers),
+                  int(layer_stride_bytes))
+
+
+def pd_kv_append(k_new, v_new, k_pool, v_pool, new_indptr, kv_len, page_indptr, page_indices, *,
+                 max_kv_len=None, dev_status=None, stream=None):
+    """Write new tokens' K/V rows ([total_new][Hkv][D]) into their page slots, in place."""
+    lib = load_library()
+    desc = _kv_desc(k_pool)
+    batch = make_batch(kv_len, page_indptr, page_indices, k_pool.shape[0], qo_indptr=_i32(new_indptr, "new_indptr"),
+                       total_qo=k_new.shape[0], max_kv_len=max_kv_len)
+    rc = lib.pd_kv_append(ctypes.byref(desc), ctypes.byref(batch), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+                          _ptr(v_pool), _ptr(dev_status), _stream(stream))
+    _check(rc, "pd_kv_append")
+
+
+def _layers(pools):
+    if pools.dim() == 5:
+        return pools.shape[0], pools[0].numel() * pools.element_size(), pools.shape[1]
+    return 1, 0, pools.shape[0]
+
+
+def pd_kv_pack(k_pools, v_pools, kv_len, page_indptr, page_indices, dst, dst_offsets, *, max_kv_len=None,
+               dev_status=None, stream=None):
+    """Gather every request's KV of all layers into dst (uint8) at dst_offsets (int64 bytes)."""
+    lib = load_library()
+    L, stride, num_pages = _layers(k_pools)
+    desc = _kv_desc(k_pools, L, stride)
+    batch = make_batch(kv_len, page_indptr, page_indices, num_pages, max_kv_len=max_kv_len)
+    rc = lib.pd_kv_pack(ctypes.byref(desc), ctypes.byref(batch), _ptr(k_pools), _ptr(v_pools), _ptr(dst),
+                        dst.numel() * dst.element_size(), _ptr(dst_offsets), _ptr(dev_status), _stream(stream))
+    _check(rc, "pd_kv_pack")
+
+
+def pd_kv_unpack(src, src_offsets, k_pools, v_pools, kv_len, page_indptr, page_indices, *, max_kv_len=None,
+                 dev_status=None, stream=None):
+    """Scatter packed per-request KV blocks into [L][num_pages][Hkv][P][D] pools, in place."""
+    lib = load_library()
+    L, stride, num_pages = _layers(k_pools)
+    desc = _kv_desc(k_pools, L, stride)
+    batch = make_batch(kv_len, page_indptr, page_indices, num_pages, max_kv_len=max_kv_len)
+    rc = lib.pd_kv_unpack(ctypes.byref(desc), ctypes.byref(batch), _ptr(src), src.numel() * src.element_size(),
+                          _ptr(src_offsets), _ptr(k_pools), _ptr(v_pools), _ptr(dev_status), _stream(stream))
+    _check(rc, "pd_kv_unpack")
+
+
+def packed_bytes(kv_len_host, num_layers, num_kv_heads, head_dim, elem_size) -> int:
+    """Bytes of the packed handoff buffer for the given per-request lengths."""
+    return int(sum(int(n) for n in kv_len_host)) * 2 * num_layers * num_kv_heads * head_dim * elem_size

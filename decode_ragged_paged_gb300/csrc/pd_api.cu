@@ -1,0 +1,260 @@
+// pd_api.cu -- the C ABI declared in include/pd.h: host-side argument checks,
+// workspace layout and dispatch to the kernel launchers. No entry point
+// allocates device memory, synchronises the stream or throws.
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "pd_internal.h"
+
+namespace pd {
+
+int device_sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64) {
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_size(int32_t dtype) { return dtype == PD_BF16 ? 2 : dtype == PD_F32 ? 4 : 0; }
+
+// Host-side checks shared by the attention entry points.
+int check_attn(const pd_attn_desc* d, const pd_batch* b, bool need_qo_indptr) {
+  if (d == nullptr || b == nullptr) return PD_ERR_INVALID_ARG;
+  if (d->num_qo_heads <= 0 || d->num_kv_heads <= 0 || d->num_qo_heads % d->num_kv_heads != 0)
+    return PD_ERR_INVALID_ARG;
+  if (d->page_size <= 0 || d->head_dim <= 0) return PD_ERR_INVALID_ARG;
+  if (elem_size(d->kv_dtype) == 0 || elem_size(d->o_dtype) == 0) return PD_ERR_INVALID_ARG;
+  if (d->layout != PD_LAYOUT_HND) return PD_ERR_UNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 128) return PD_ERR_UNSUPPORTED;
+  if (!(d->sm_scale <= 0.f || isfinite(d->sm_scale))) return PD_ERR_INVALID_ARG;
+  if (b->batch_size < 0 || b->total_qo < 0 || b->max_qo_len < 0 || b->max_kv_len < 0) return PD_ERR_INVALID_ARG;
+  if (b->batch_size > 0) {
+    if (b->kv_len == nullptr || b->page_indptr == nullptr || b->page_indices == nullptr) return PD_ERR_INVALID_ARG;
+    if (need_qo_indptr && b->qo_indptr == nullptr) return PD_ERR_INVALID_ARG;
+    if (b->num_pages <= 0) return PD_ERR_INVALID_ARG;
+  }
+  return PD_OK;
+}
+
+float scale_of(const pd_attn_desc* d) {
+  return d->sm_scale > 0.f ? d->sm_scale : 1.0f / sqrtf((float)d->head_dim);
+}
+
+DecodeLayout decode_layout_for(const pd_attn_desc* d, const pd_batch* b) {
+  const int gs = decode_heads_per_item(d->num_qo_heads / d->num_kv_heads, d->head_dim);
+  return decode_layout(b->batch_size, d->num_qo_heads, d->head_dim, b->max_kv_len, d->num_qo_heads / gs,
+                       device_sm_count());
+}
+
+}  // namespace
+}  // namespace pd
+
+using namespace pd;
+
+extern "C" {
+
+int32_t pd_version(void) { return 100; }
+
+const char* pd_status_string(int32_t code) {
+  switch (code) {
+    case PD_OK: return "ok";
+    case PD_ERR_INVALID_ARG: return "invalid argument";
+    case PD_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PD_ERR_WORKSPACE: return "workspace too small";
+    case PD_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+const char* pd_device_status_string(int32_t code) {
+  switch (code) {
+    case PD_DEV_OK: return "ok";
+    case PD_DEV_BAD_INDPTR: return "indptr decreasing or out of range";
+    case PD_DEV_BAD_LENGTH: return "length out of range";
+    case PD_DEV_BAD_PAGE_TABLE: return "page table too short or page id out of range";
+    case PD_DEV_NOT_DECODE: return "decode request with qo_len != 1";
+    case PD_DEV_TIMEOUT: return "bounded wait timed out inside a kernel";
+    case PD_DEV_BAD_OFFSET: return "pack/unpack block misaligned or outside the packed buffer";
+    default: return "unknown device status";
+  }
+}
+
+size_t pd_attn_workspace_size(const pd_attn_desc* desc, const pd_batch* batch, int32_t kind) {
+  if (check_attn(desc, batch, false) != PD_OK) return 0;
+  if (kind == PD_KIND_DECODE) return decode_layout_for(desc, batch).total;
+  return 0;
+}
+
+int pd_attn_decode(const pd_attn_desc* desc, const pd_batch* batch, const void* q, const void* k_pool,
+                   const void* v_pool, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                   int32_t* dev_status, void* stream) {
+  int rc = check_attn(desc, batch, false);
+  if (rc != PD_OK) return rc;
+  if (batch->batch_size == 0) return PD_OK;
+  if (q == nullptr || k_pool == nullptr || v_pool == nullptr || o == nullptr || workspace == nullptr)
+    return PD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o) || !aligned16(workspace))
+    return PD_ERR_INVALID_ARG;
+  if (batch->qo_indptr == nullptr && batch->total_qo < batch->batch_size) return PD_ERR_INVALID_ARG;
+  const DecodeLayout L = decode_layout_for(desc, batch);
+  if (workspace_bytes < L.total) return PD_ERR_WORKSPACE;
+
+  DecodeParams p{};
+  p.batch = batch->batch_size;
+  p.hq = desc->num_qo_heads;
+  p.hkv = desc->num_kv_heads;
+  p.head_dim = desc->head_dim;
+  p.page_size = desc->page_size;
+  p.group = p.hq / p.hkv;
+  p.heads_per_item = decode_heads_per_item(p.group, p.head_dim);
+  p.items_per_chunk = p.hq / p.heads_per_item;
+  p.total_qo = batch->total_qo;
+  p.max_kv_len = batch->max_kv_len;
+  p.num_pages = batch->num_pages;
+  p.chunk_target = L.chunk_target;
+  p.max_chunks = L.max_chunks;
+  p.o_dtype = desc->o_dtype;
+  p.scale_log2 = scale_of(desc) * kLog2e;
+  p.qo_indptr = batch->qo_indptr;
+  p.kv_len = batch->kv_len;
+  p.page_indptr = batch->page_indptr;
+  p.page_indices = batch->page_indices;
+  p.q = q;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.o = o;
+  p.lse = lse;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
+  p.req_info = reinterpret_cast<int4*>(ws + L.req_info);
+  p.rc_list = reinterpret_cast<int2*>(ws + L.rc_list);
+  p.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  p.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  p.status = dev_status;
+  return launch_decode(p, desc->kv_dtype, static_cast<cudaStream_t>(stream));
+}
+
+int pd_attn_prefill(const pd_attn_desc* desc, const pd_batch* batch, const void* q, const void* k_pool,
+                    const void* v_pool, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                    int32_t* dev_status, void* stream) {
+  (void)q; (void)k_pool; (void)v_pool; (void)o; (void)lse; (void)workspace; (void)workspace_bytes;
+  (void)dev_status; (void)stream;
+  const int rc = check_attn(desc, batch, true);
+  if (rc != PD_OK) return rc;
+  return PD_ERR_UNSUPPORTED;
+}
+
+int pd_attn_mixed(const pd_attn_desc* desc, const pd_batch* batch, const void* q, const void* k_pool,
+                  const void* v_pool, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                  int32_t* dev_status, void* stream) {
+  (void)q; (void)k_pool; (void)v_pool; (void)o; (void)lse; (void)workspace; (void)workspace_bytes;
+  (void)dev_status; (void)stream;
+  const int rc = check_attn(desc, batch, true);
+  if (rc != PD_OK) return rc;
+  return PD_ERR_UNSUPPORTED;
+}
+
+namespace {
+
+int check_kv(const pd_kv_desc* d, const pd_batch* b) {
+  if (d == nullptr || b == nullptr) return PD_ERR_INVALID_ARG;
+  const int es = elem_size(d->dtype);
+  if (es == 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 || d->page_size <= 0 || d->num_layers <= 0)
+    return PD_ERR_INVALID_ARG;
+  if (d->layout != PD_LAYOUT_HND) return PD_ERR_UNSUPPORTED;
+  if ((d->head_dim * es) % 16 != 0) return PD_ERR_UNSUPPORTED;
+  if (d->num_layers > 1 && (d->layer_stride_bytes <= 0 || d->layer_stride_bytes % 16 != 0))
+    return PD_ERR_INVALID_ARG;
+  if (b->batch_size < 0 || b->max_kv_len < 0 || b->total_qo < 0) return PD_ERR_INVALID_ARG;
+  if (b->batch_size > 0) {
+    if (b->kv_len == nullptr || b->page_indptr == nullptr || b->page_indices == nullptr) return PD_ERR_INVALID_ARG;
+    if (b->num_pages <= 0) return PD_ERR_INVALID_ARG;
+  }
+  return PD_OK;
+}
+
+KvCopyParams kv_params(const pd_kv_desc* d, const pd_batch* b, int32_t* status) {
+  KvCopyParams p{};
+  p.batch = b->batch_size;
+  p.hkv = d->num_kv_heads;
+  p.head_dim = d->head_dim;
+  p.page_size = d->page_size;
+  p.num_layers = d->num_layers;
+  p.num_pages = b->num_pages;
+  p.elem_size = elem_size(d->dtype);
+  p.max_kv_len = b->max_kv_len;
+  p.max_new = b->total_qo;
+  p.layer_stride = d->layer_stride_bytes;
+  p.new_indptr = b->qo_indptr;
+  p.kv_len = b->kv_len;
+  p.page_indptr = b->page_indptr;
+  p.page_indices = b->page_indices;
+  p.status = status;
+  return p;
+}
+
+}  // namespace
+
+int pd_kv_append(const pd_kv_desc* desc, const pd_batch* batch, const void* k_new, const void* v_new,
+                 void* k_pool, void* v_pool, int32_t* dev_status, void* stream) {
+  int rc = check_kv(desc, batch);
+  if (rc != PD_OK) return rc;
+  if (desc->num_layers != 1) return PD_ERR_INVALID_ARG;
+  if (batch->batch_size == 0 || batch->total_qo == 0) return PD_OK;
+  if (batch->qo_indptr == nullptr || k_new == nullptr || v_new == nullptr || k_pool == nullptr || v_pool == nullptr)
+    return PD_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool)) return PD_ERR_INVALID_ARG;
+  KvCopyParams p = kv_params(desc, batch, dev_status);
+  p.src = k_new;
+  p.src2 = v_new;
+  p.dst = k_pool;
+  p.dst2 = v_pool;
+  return launch_kv_append(p, static_cast<cudaStream_t>(stream));
+}
+
+int pd_kv_pack(const pd_kv_desc* desc, const pd_batch* batch, const void* k_pool, const void* v_pool, void* dst,
+               size_t dst_bytes, const int64_t* dst_offsets, int32_t* dev_status, void* stream) {
+  int rc = check_kv(desc, batch);
+  if (rc != PD_OK) return rc;
+  if (batch->batch_size == 0) return PD_OK;
+  if (k_pool == nullptr || v_pool == nullptr || dst == nullptr || dst_offsets == nullptr) return PD_ERR_INVALID_ARG;
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(dst)) return PD_ERR_INVALID_ARG;
+  KvCopyParams p = kv_params(desc, batch, dev_status);
+  p.src = k_pool;
+  p.src2 = v_pool;
+  p.dst = dst;
+  p.offsets = dst_offsets;
+  p.buf_bytes = (int64_t)dst_bytes;
+  return launch_kv_pack(p, static_cast<cudaStream_t>(stream));
+}
+
+int pd_kv_unpack(const pd_kv_desc* desc, const pd_batch* batch, const void* src, size_t src_bytes,
+                 const int64_t* src_offsets, void* k_pool, void* v_pool, int32_t* dev_status, void* stream) {
+  int rc = check_kv(desc, batch);
+  if (rc != PD_OK) return rc;
+  if (batch->batch_size == 0) return PD_OK;
+  if (k_pool == nullptr || v_pool == nullptr || src == nullptr || src_offsets == nullptr) return PD_ERR_INVALID_ARG;
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(src)) return PD_ERR_INVALID_ARG;
+  KvCopyParams p = kv_params(desc, batch, dev_status);
+  p.src = src;
+  p.dst = k_pool;
+  p.dst2 = v_pool;
+  p.offsets = src_offsets;
+  p.buf_bytes = (int64_t)src_bytes;
+  return launch_kv_unpack(p, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// pd_internal.h -- launch parameters and launcher declarations shared between
+// the C-ABI layer (pd_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pd.h"
+
+namespace pd {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ------------------------------------------------------------------ decode
+// Workspace of the split-KV decode (all offsets 256-byte aligned):
+//   hdr       int32[64]            hdr[0] = work items, hdr[1] = chunks in total
+//   req_info  int4[B]              {first chunk, chunks, chunk length, q row or -1 if skipped}
+//   rc_list   int2[max_chunks]     (request, chunk index) of every chunk
+//   part_o    float[max_chunks][Hq][D]   normalised partial outputs
+//   part_lse  float[max_chunks][Hq]      their log2-sum-exp2 of scaled scores
+struct DecodeParams {
+  int32_t batch, hq, hkv, head_dim, page_size, group, heads_per_item, items_per_chunk;
+  int32_t total_qo, max_kv_len, num_pages, chunk_target, max_chunks;
+  int32_t o_dtype;
+  float scale_log2;  // softmax scale times log2(e)
+  const int32_t* qo_indptr;  // may be null: row r = request r
+  const int32_t* kv_len;
+  const int32_t* page_indptr;
+  const int32_t* page_indices;
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  void* o;
+  float* lse;
+  int32_t* hdr;
+  int4* req_info;
+  int2* rc_list;
+  float* part_o;
+  float* part_lse;
+  int32_t* status;
+};
+
+struct DecodeLayout {
+  size_t hdr, req_info, rc_list, part_o, part_lse, total;
+  int32_t chunk_target, max_chunks;
+};
+
+// Chunk length and workspace layout of a decode over `batch` requests of at
+// most max_kv_len tokens; `sm_count` sizes the split.
+DecodeLayout decode_layout(int32_t batch, int32_t hq, int32_t head_dim, int32_t max_kv_len,
+                           int32_t items_per_chunk, int32_t sm_count);
+
+// Heads of one group processed together by a decode work item.
+int32_t decode_heads_per_item(int32_t group, int32_t head_dim);
+
+// Plans and runs a decode. Returns a pd_status.
+int launch_decode(DecodeParams& p, int32_t kv_dtype, cudaStream_t stream);
+
+// --------------------------------------------------------------- KV copies
+struct KvCopyParams {
+  int32_t batch, hkv, head_dim, page_size, num_layers, num_pages, elem_size;
+  int32_t max_kv_len, max_new;
+  int64_t layer_stride;
+  const int32_t* new_indptr;   // append only
+  const int32_t* kv_len;
+  const int32_t* page_indptr;
+  const int32_t* page_indices;
+  const void* src;             // append: k_new; pack: k pool; unpack: packed buffer
+  const void* src2;            // append: v_new; pack: v pool
+  void* dst;                   // append: k pool; pack: packed buffer; unpack: k pool
+  void* dst2;                  // append: v pool; unpack: v pool
+  const int64_t* offsets;      // pack: dst offsets; unpack: src offsets
+  int64_t buf_bytes;           // size of the packed buffer
+  int32_t* status;
+};
+
+int launch_kv_append(const KvCopyParams& p, cudaStream_t stream);
+int launch_kv_pack(const KvCopyParams& p, cudaStream_t stream);
+int launch_kv_unpack(const KvCopyParams& p, cudaStream_t stream);
+
+// ------------------------------------------------------------------- misc
+int device_sm_count();
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace pd

@@ -1,0 +1,232 @@
+// pd_kvcopy.cu -- KV-cache append and the page pack / unpack of the KV handoff.
+//
+// Perplexity, "Disaggregated prefill and decode" (2025):
+//   section "KV Messenger": page copies of a layer start as soon as the model
+//   has appended that layer's KV entries to the cache;
+//   section "Sharded KV cache transfers" and its figure on NHD/HND layouts: with
+//   the HND layout each head's slice of a page is contiguous, so a page slice
+//   moves as one run; when prefiller and decoder cut pages differently, pages
+//   are split or rebuilt.
+//
+// All three are pure byte moves, bound by HBM bandwidth. Each unit of work is a
+// contiguous run on both sides and is copied by one warp with 16-byte vector
+// loads, several in flight per lane.
+#include "pd_common.cuh"
+#include "pd_internal.h"
+
+namespace pd {
+
+namespace {
+
+constexpr int kCopyThreads = 256;
+constexpr int kUnroll = 8;  // 16-byte vectors in flight per lane
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// One warp copies nvec 16-byte vectors from src to dst.
+__device__ __forceinline__ void warp_copy(const uint4* __restrict__ src, uint4* __restrict__ dst, int nvec,
+                                          int lane) {
+  for (int base = 0; base < nvec; base += 32 * kUnroll) {
+    uint4 t[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = base + u * 32 + lane;
+      if (i < nvec) t[u] = ld_stream(src + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = base + u * 32 + lane;
+      if (i < nvec) st_stream(dst + i, t[u]);
+    }
+  }
+}
+
+// Unit u of a pack / unpack enumerates (request r, layer, K/V, head h, page k of
+// the request) with k fastest, so consecutive warps touch consecutive bytes of
+// the packed buffer. Page k carries tokens [k*P, min((k+1)*P, kv_len)).
+struct Unit {
+  int r, layer, kv, h, k;
+};
+
+__device__ __forceinline__ Unit unit_of(int64_t u, int kp, int hkv, int layers) {
+  Unit x;
+  x.k = (int)(u % kp);
+  u /= kp;
+  x.h = (int)(u % hkv);
+  u /= hkv;
+  x.kv = (int)(u % 2);
+  u /= 2;
+  x.layer = (int)(u % layers);
+  x.r = (int)(u / layers);
+  return x;
+}
+
+}  // namespace
+
+// --------------------------------------------------------------- append
+// One CTA per new-token row at a time: all heads of K and V of that row.
+__global__ void __launch_bounds__(kCopyThreads) kv_append_kernel(const KvCopyParams p) {
+  const int row_bytes = p.head_dim * p.elem_size;
+  const int vpr = row_bytes / 16;               // vectors per (token, head) row
+  const int per_row = 2 * p.hkv * vpr;          // vectors of K and V of one token
+  const int total_rows = p.max_new;             // rows of k_new / v_new
+  for (int row = blockIdx.x; row < total_rows; row += gridDim.x) {
+    // request owning the row: last r with new_indptr[r] <= row
+    int lo = 0, hi = p.batch;  // answer in [lo, hi)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.new_indptr + mid) <= row) lo = mid;
+      else hi = mid;
+    }
+    const int r = lo;
+    const int a = __ldg(p.new_indptr + r), b = __ldg(p.new_indptr + r + 1);
+    if (row < a || row >= b) continue;  // row past the last request's tokens
+    const int n_new = b - a, n = __ldg(p.kv_len + r);
+    const int pa = __ldg(p.page_indptr + r), pb = __ldg(p.page_indptr + r + 1);
+    const int t = n - n_new + (row - a);
+    bool ok = n_new <= n && n <= p.max_kv_len && pa >= 0 && pb >= pa &&
+              (int64_t)(pb - pa) * p.page_size >= n;
+    int32_t page = 0;
+    if (ok) {
+      page = __ldg(p.page_indices + pa + t / p.page_size);
+      ok = page >= 0 && page < p.num_pages;
+      if (!ok && threadIdx.x == 0) report(p.status, PD_DEV_BAD_PAGE_TABLE);
+    } else if (threadIdx.x == 0) {
+      report(p.status, PD_DEV_BAD_LENGTH);
+    }
+    if (!ok) continue;
+    const int slot = t % p.page_size;
+    uint4 tmp[kUnroll];
+    // Every thread loads its vectors first, then stores them.
+    for (int base = 0; base < per_row; base += kCopyThreads * kUnroll) {
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int i = base + u * kCopyThreads + threadIdx.x;
+        if (i < per_row) {
+          const int kv = i / (p.hkv * vpr);
+          const int rem = i - kv * p.hkv * vpr;
+          const uint4* src = static_cast<const uint4*>(kv ? p.src2 : p.src) + (int64_t)row * p.hkv * vpr + rem;
+          tmp[u] = ld_stream(src);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int i = base + u * kCopyThreads + threadIdx.x;
+        if (i < per_row) {
+          const int kv = i / (p.hkv * vpr);
+          const int rem = i - kv * p.hkv * vpr;
+          const int h = rem / vpr, v = rem - h * vpr;
+          uint4* dst = static_cast<uint4*>(kv ? p.dst2 : p.dst) +
+                       (((int64_t)page * p.hkv + h) * p.page_size + slot) * vpr + v;
+          *dst = tmp[u];
+        }
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------------- pack
+__global__ void __launch_bounds__(kCopyThreads) kv_pack_kernel(const KvCopyParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = ((int64_t)blockIdx.x * kCopyThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kCopyThreads) >> 5;
+  const int kp = (p.max_kv_len + p.page_size - 1) / p.page_size;
+  const int64_t units = (int64_t)p.batch * p.num_layers * 2 * p.hkv * kp;
+  const int vpr = p.head_dim * p.elem_size / 16;
+  for (int64_t u = warp0; u < units; u += nwarps) {
+    const Unit x = unit_of(u, kp, p.hkv, p.num_layers);
+    const int n = __ldg(p.kv_len + x.r);
+    if ((int64_t)x.k * p.page_size >= n) continue;
+    const int pa = __ldg(p.page_indptr + x.r), pb = __ldg(p.page_indptr + x.r + 1);
+    const int64_t off = __ldg(p.offsets + x.r);
+    const int64_t block = (int64_t)p.num_layers * 2 * p.hkv * n * vpr * 16;
+    const bool bad_off = (off & 15) != 0 || off < 0 || off + block > p.buf_bytes;
+    if (n > p.max_kv_len || pa < 0 || (int64_t)(pb - pa) * p.page_size < n || bad_off) {
+      if (lane == 0) report(p.status, bad_off ? PD_DEV_BAD_OFFSET : PD_DEV_BAD_PAGE_TABLE);
+      continue;
+    }
+    const int32_t page = __ldg(p.page_indices + pa + x.k);
+    if (page < 0 || page >= p.num_pages) {
+      if (lane == 0) report(p.status, PD_DEV_BAD_PAGE_TABLE);
+      continue;
+    }
+    const int rows = min(p.page_size, n - x.k * p.page_size);
+    const uint8_t* pool = static_cast<const uint8_t*>(x.kv ? p.src2 : p.src) + (int64_t)x.layer * p.layer_stride;
+    const uint4* src = reinterpret_cast<const uint4*>(pool) + ((int64_t)page * p.hkv + x.h) * p.page_size * vpr;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dst) + off) +
+                 ((((int64_t)x.layer * 2 + x.kv) * p.hkv + x.h) * n + (int64_t)x.k * p.page_size) * vpr;
+    warp_copy(src, dst, rows * vpr, lane);
+  }
+}
+
+// --------------------------------------------------------------- unpack
+__global__ void __launch_bounds__(kCopyThreads) kv_unpack_kernel(const KvCopyParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = ((int64_t)blockIdx.x * kCopyThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kCopyThreads) >> 5;
+  const int kp = (p.max_kv_len + p.page_size - 1) / p.page_size;
+  const int64_t units = (int64_t)p.batch * p.num_layers * 2 * p.hkv * kp;
+  const int vpr = p.head_dim * p.elem_size / 16;
+  for (int64_t u = warp0; u < units; u += nwarps) {
+    const Unit x = unit_of(u, kp, p.hkv, p.num_layers);
+    const int n = __ldg(p.kv_len + x.r);
+    if ((int64_t)x.k * p.page_size >= n) continue;
+    const int pa = __ldg(p.page_indptr + x.r), pb = __ldg(p.page_indptr + x.r + 1);
+    const int64_t off = __ldg(p.offsets + x.r);
+    const int64_t block = (int64_t)p.num_layers * 2 * p.hkv * n * vpr * 16;
+    const bool bad_off = (off & 15) != 0 || off < 0 || off + block > p.buf_bytes;
+    if (n > p.max_kv_len || pa < 0 || (int64_t)(pb - pa) * p.page_size < n || bad_off) {
+      if (lane == 0) report(p.status, bad_off ? PD_DEV_BAD_OFFSET : PD_DEV_BAD_PAGE_TABLE);
+      continue;
+    }
+    const int32_t page = __ldg(p.page_indices + pa + x.k);
+    if (page < 0 || page >= p.num_pages) {
+      if (lane == 0) report(p.status, PD_DEV_BAD_PAGE_TABLE);
+      continue;
+    }
+    const int rows = min(p.page_size, n - x.k * p.page_size);
+    uint8_t* pool = static_cast<uint8_t*>(x.kv ? p.dst2 : p.dst) + (int64_t)x.layer * p.layer_stride;
+    uint4* dst = reinterpret_cast<uint4*>(pool) + ((int64_t)page * p.hkv + x.h) * p.page_size * vpr;
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.src) + off) +
+                       ((((int64_t)x.layer * 2 + x.kv) * p.hkv + x.h) * n + (int64_t)x.k * p.page_size) * vpr;
+    warp_copy(src, dst, rows * vpr, lane);
+  }
+}
+
+// ----------------------------------------------------------------- host
+namespace {
+int copy_grid() { return device_sm_count() * (2048 / kCopyThreads); }
+}  // namespace
+
+int launch_kv_append(const KvCopyParams& p, cudaStream_t stream) {
+  if (p.max_new <= 0 || p.batch <= 0) return PD_OK;
+  int grid = copy_grid();
+  if (grid > p.max_new) grid = p.max_new;
+  kv_append_kernel<<<grid, kCopyThreads, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
+}
+
+int launch_kv_pack(const KvCopyParams& p, cudaStream_t stream) {
+  if (p.batch <= 0 || p.max_kv_len <= 0) return PD_OK;
+  kv_pack_kernel<<<copy_grid(), kCopyThreads, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
+}
+
+int launch_kv_unpack(const KvCopyParams& p, cudaStream_t stream) {
+  if (p.batch <= 0 || p.max_kv_len <= 0) return PD_OK;
+  kv_unpack_kernel<<<copy_grid(), kCopyThreads, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
+}
+
+}  // namespace pd

@@ -1,0 +1,236 @@
+/*
+ * pd.h -- C ABI of the paged ragged-attention and KV-handoff library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The library implements the single-GPU hot path behind disaggregated
+ * prefill/decode serving described in Perplexity, "Disaggregated prefill and
+ * decode" (2025):
+ *   - attention over a paged KV cache for ragged batches of decode requests
+ *     (qo_len = 1, long kv_len), causal prefill requests (large qo_len) and
+ *     mixed batches of both (section "Prefill vs Decode performance");
+ *   - appending a layer's new K/V entries into their pages, after which that
+ *     layer's pages may be shipped (section "KV Messenger");
+ *   - packing a finished prefill's pages into a contiguous buffer and unpacking
+ *     them into a decoder's pool with a different page size and page table
+ *     (section "Sharded KV cache transfers").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Memory. Every pointer argument named "device" points to GPU memory owned by
+ * the caller; the library allocates nothing per call and keeps no pointer after
+ * a call returns. All work is enqueued on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream) and runs asynchronously: buffers must stay alive until
+ * the stream has passed the call. Descriptor structs are read on the host
+ * during the call only.
+ *
+ * Pool layout (HND, "head before token", from the post's figure on NHD and HND
+ * KV-cache layouts): a pool is [num_pages][num_kv_heads][page_size][head_dim],
+ * row-major, so each head's slice of a page is one contiguous run of
+ * page_size * head_dim elements. K and V live in two pools that share one page
+ * table. Pools must be 16-byte aligned.
+ *
+ * Page table (CSR): request r owns pages
+ * page_indices[page_indptr[r] .. page_indptr[r+1]); logical token t of r sits in
+ * page page_indices[page_indptr[r] + t / page_size], slot t % page_size.
+ *
+ * Ragged rows: q and o are [total_qo][num_qo_heads][head_dim]; the rows of
+ * request r are qo_indptr[r] .. qo_indptr[r+1]. kv_len[r] counts all of r's
+ * cached tokens including the new ones, so the new rows are the last qo_len
+ * positions (bottom-right causal alignment: row i may attend keys
+ * j <= kv_len - qo_len + i).
+ *
+ * Grouped-query attention (section "Qwen3-Coder"): num_kv_heads divides
+ * num_qo_heads; query head h reads KV head h / (num_qo_heads / num_kv_heads).
+ *
+ * Errors. Host-side checks run first; on failure a negative pd_status is
+ * returned and nothing is enqueued. Checks of device-resident data (indptr
+ * monotonicity, lengths against the host bounds, page ids against num_pages)
+ * run on the GPU: a request that fails one is skipped (its outputs are left
+ * unspecified) and, when `dev_status` is not NULL, the first failure's
+ * pd_device_status code is stored there with an atomic compare-and-swap from 0
+ * (the caller zeroes it and reads it back when it wants to know). No call
+ * faults the GPU on bad table contents; every wait inside a kernel is bounded
+ * and reports PD_DEV_TIMEOUT instead of hanging.
+ *
+ * Thread safety: calls are stateless apart from per-device launch attributes
+ * cached on first use; distinct streams may call concurrently with distinct
+ * workspaces.
+ */
+#ifndef PD_H_
+#define PD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PD_API __attribute__((visibility("default")))
+#else
+#define PD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes of every entry point. */
+typedef enum {
+  PD_OK = 0,
+  PD_ERR_INVALID_ARG = -1, /* null pointer, negative or inconsistent host-side size */
+  PD_ERR_UNSUPPORTED = -2, /* valid request this build does not implement */
+  PD_ERR_WORKSPACE = -3,   /* workspace smaller than pd_attn_workspace_size() */
+  PD_ERR_CUDA = -4         /* a CUDA runtime call or kernel launch failed */
+} pd_status;
+
+/* Codes stored into *dev_status by the kernels (first failure wins). */
+typedef enum {
+  PD_DEV_OK = 0,
+  PD_DEV_BAD_INDPTR = 1,     /* qo_indptr / page_indptr decreasing or past total_qo */
+  PD_DEV_BAD_LENGTH = 2,     /* kv_len < 0, > max_kv_len, qo_len > max_qo_len, or causal qo_len > kv_len */
+  PD_DEV_BAD_PAGE_TABLE = 3, /* fewer pages than ceil(kv_len / page_size), or a page id outside [0, num_pages) */
+  PD_DEV_NOT_DECODE = 4,     /* pd_attn_decode given a request with qo_len != 1 */
+  PD_DEV_TIMEOUT = 5,        /* a bounded wait inside a kernel ran out; the kernel returned early */
+  PD_DEV_BAD_OFFSET = 6      /* a pack / unpack block misaligned or outside the packed buffer */
+} pd_device_status;
+
+typedef enum { PD_F32 = 0, PD_BF16 = 1 } pd_dtype;
+
+typedef enum { PD_LAYOUT_HND = 0 } pd_layout;
+
+typedef enum { PD_KIND_DECODE = 0, PD_KIND_PREFILL = 1, PD_KIND_MIXED = 2 } pd_attn_kind;
+
+/* Shape and numerics of one attention call. */
+typedef struct {
+  int32_t num_qo_heads; /* Hq */
+  int32_t num_kv_heads; /* Hkv; must divide Hq */
+  int32_t head_dim;     /* D: 64 or 128 */
+  int32_t page_size;    /* P: tokens per page, >= 1 */
+  int32_t kv_dtype;     /* pd_dtype of q, k_pool and v_pool */
+  int32_t o_dtype;      /* pd_dtype of o */
+  int32_t layout;       /* pd_layout; PD_LAYOUT_HND */
+  int32_t causal;       /* 1: bottom-right causal mask; 0: every row sees all kv_len keys */
+  float sm_scale;       /* softmax scale; <= 0 selects 1/sqrt(head_dim) */
+} pd_attn_desc;
+
+/* A ragged batch. Device arrays are int32. */
+typedef struct {
+  int32_t batch_size;          /* B >= 0 */
+  const int32_t *qo_indptr;    /* device [B+1]; NULL in pd_attn_decode means row r = request r */
+  const int32_t *kv_len;       /* device [B] */
+  const int32_t *page_indptr;  /* device [B+1] */
+  const int32_t *page_indices; /* device [page_indptr[B]] */
+  int32_t num_pages;           /* pages in each pool (bound for page ids) */
+  int32_t total_qo;            /* host: rows of q and o, qo_indptr[B] */
+  int32_t max_qo_len;          /* host: bound on every qo_len (sizes grids and workspace) */
+  int32_t max_kv_len;          /* host: bound on every kv_len (sizes grids and workspace) */
+} pd_batch;
+
+/* Shape of KV pools for append / pack / unpack. */
+typedef struct {
+  int32_t num_kv_heads;       /* Hkv */
+  int32_t head_dim;           /* D; head_dim * element size must be a multiple of 16 bytes */
+  int32_t page_size;          /* P >= 1 */
+  int32_t dtype;              /* pd_dtype of the pools */
+  int32_t layout;             /* PD_LAYOUT_HND */
+  int32_t num_layers;         /* L >= 1 (append: the layer count is 1) */
+  int64_t layer_stride_bytes; /* bytes from layer l's pool to layer l+1's; same for K and V */
+} pd_kv_desc;
+
+/*
+ * Bytes of device workspace an attention call of `kind` needs for this
+ * descriptor and the batch's host-side sizes (batch_size, total_qo, max_qo_len,
+ * max_kv_len). 16-byte alignment required. Returns 0 when the arguments are
+ * invalid. The workspace carries the per-call plan and the split-KV partial
+ * results; it needs no initialisation and may be reused once a previous call
+ * using it has finished on the GPU.
+ */
+PD_API size_t pd_attn_workspace_size(const pd_attn_desc *desc, const pd_batch *batch, int32_t kind);
+
+/*
+ * Decode attention (section "Prefill vs Decode performance": qo_len = 1 per
+ * request, attention parallelised over requests and over kv_len).
+ *   q        device [B][Hq][D] (kv_dtype)
+ *   k_pool   device [num_pages][Hkv][P][D] (kv_dtype), v_pool likewise
+ *   o        device [B][Hq][D] (o_dtype): softmax(q K^T * scale) V
+ *   lse      device [B][Hq] fp32, natural-log log-sum-exp of the scaled scores;
+ *            may be NULL. A request with kv_len = 0 gives o = 0, lse = -inf.
+ *   workspace / workspace_bytes: see pd_attn_workspace_size(kind = PD_KIND_DECODE)
+ *   dev_status: device int32 or NULL (see "Errors" above)
+ * The KV axis is split into chunks processed by separate CTAs; the partial
+ * results are merged by log-sum-exp. Supported: kv_dtype f32 or bf16, D 64 or
+ * 128, any page size, any group size Hq/Hkv. The causal flag is irrelevant for
+ * one row per request.
+ */
+PD_API int pd_attn_decode(const pd_attn_desc *desc, const pd_batch *batch, const void *q,
+                   const void *k_pool, const void *v_pool, void *o, float *lse,
+                   void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * Prefill attention: any qo_len <= kv_len per request, causal or not (section
+ * "Prefill vs Decode performance": prefill requests bring many tokens and are
+ * compute bound). Arguments as pd_attn_decode with q, o [total_qo][Hq][D]
+ * and lse [total_qo][Hq]. Supported: kv_dtype bf16, D 128; tensor-core tiles
+ * of 128 query rows.
+ */
+PD_API int pd_attn_prefill(const pd_attn_desc *desc, const pd_batch *batch, const void *q,
+                    const void *k_pool, const void *v_pool, void *o, float *lse,
+                    void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * Mixed batch in one launch: requests with qo_len = 1 take the split-KV decode
+ * path, the others the prefill path (section "Prefill vs Decode performance":
+ * mixing prefill into decode batches). Arguments and support as
+ * pd_attn_prefill.
+ */
+PD_API int pd_attn_mixed(const pd_attn_desc *desc, const pd_batch *batch, const void *q,
+                  const void *k_pool, const void *v_pool, void *o, float *lse,
+                  void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * KV append (section "KV Messenger": page copies of a layer start once the
+ * model has appended that layer's KV entries). The batch's qo_indptr counts
+ * the new tokens: request r brings n_r = qo_indptr[r+1] - qo_indptr[r] rows of
+ * k_new / v_new ([total_qo][Hkv][D], device) that land at logical positions
+ * kv_len[r] - n_r .. kv_len[r] - 1 of its pages in k_pool / v_pool (device,
+ * written in place). Bit-exact copy. desc->num_layers must be 1.
+ */
+PD_API int pd_kv_append(const pd_kv_desc *desc, const pd_batch *batch, const void *k_new,
+                 const void *v_new, void *k_pool, void *v_pool, int32_t *dev_status,
+                 void *stream);
+
+/*
+ * KV pack (sections "KV Messenger" and "Sharded KV cache transfers": a
+ * finished prefill's pages leave the prefiller). For every request r the
+ * kv_len[r] tokens of every layer are gathered into a contiguous block at
+ * dst + dst_offsets[r] bytes, laid out [L][2 (K, V)][Hkv][kv_len[r]][D]; with
+ * the HND layout each (page, head) slice is one contiguous run on both sides.
+ * Layer l's pools start at k_pool / v_pool + l * layer_stride_bytes (device).
+ * dst_offsets: device int64 [B], 16-byte multiples; dst_bytes: size of dst. A
+ * request whose block would not fit inside dst is skipped and reported
+ * (PD_DEV_BAD_OFFSET). Bit-exact copy. The batch's qo_indptr is ignored.
+ */
+PD_API int pd_kv_pack(const pd_kv_desc *desc, const pd_batch *batch, const void *k_pool,
+                      const void *v_pool, void *dst, size_t dst_bytes, const int64_t *dst_offsets,
+                      int32_t *dev_status, void *stream);
+
+/*
+ * KV unpack: the inverse of pd_kv_pack into a pool with its own page size and
+ * page table (section "Sharded KV cache transfers": pages are split or rebuilt
+ * when the two sides differ). Only slots of tokens t < kv_len[r] are written.
+ * src_bytes bounds the blocks read from src as dst_bytes does for pd_kv_pack.
+ */
+PD_API int pd_kv_unpack(const pd_kv_desc *desc, const pd_batch *batch, const void *src,
+                        size_t src_bytes, const int64_t *src_offsets, void *k_pool, void *v_pool,
+                        int32_t *dev_status, void *stream);
+
+/* Static description of a pd_status or pd_device_status code (never NULL). */
+PD_API const char *pd_status_string(int32_t code);
+PD_API const char *pd_device_status_string(int32_t code);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+PD_API int32_t pd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PD_H_ */

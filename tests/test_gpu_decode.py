@@ -1,0 +1,115 @@
+"""GPU parity of pd_attn_decode against the fp64 oracle (same seeded inputs).
+
+Tolerances from the benchmark spec: max |o - oracle| <= 1e-4 for fp32
+inputs, <= 1e-2 for bf16 inputs (fp32 accumulation), |lse - oracle| <= 1e-3.
+Unused pool pages and tail slots hold NaN, so a stray read shows up."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import decode_ragged_paged_gb300 as pd
+    from gpu_util import DevCase, compare
+
+
+def run_decode(case, o_dtype=None, status=None):
+    d = DevCase(case)
+    odt = None if o_dtype is None else {wl.F32: torch.float32, wl.BF16: torch.bfloat16}[o_dtype]
+    o, lse = pd.pd_attn_decode(d.q, d.k_pool, d.v_pool, d.kv_len, d.page_indptr, d.page_indices,
+                               sm_scale=case.sm_scale, max_kv_len=d.max_kv_len, o_dtype=odt,
+                               dev_status=status)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def check(case, o_dtype=None):
+    o, lse = run_decode(case, o_dtype)
+    o_ref, lse_ref = oracle.attention_case(case)
+    return compare(o, lse, o_ref, lse_ref, case.dtype)
+
+
+def test_decode_correctness_workload_fp32():
+    # 4 requests, kv_len {17, 64, 100, 255}, 8 heads, D 64, page 16, fp32, 64-page pool
+    check(wl.decode_correctness())
+
+
+def test_decode_batch_workload_bf16_full():
+    # 128 requests, kv_len U[512, 4096], GQA 32/8, D 128, page 16, bf16: every output row
+    case = wl.decode_batch()
+    err_o, err_l = check(case)
+    assert err_o < 1e-2 and err_l < 1e-3
+
+
+@pytest.mark.parametrize("o_dtype", [wl.F32, wl.BF16])
+def test_decode_output_dtypes(o_dtype):
+    case = wl.make_attn_case(101, [1] * 5, [1, 16, 17, 300, 700], 16, 4, 128, 16, wl.BF16, num_pages=80)
+    check(case, o_dtype)
+
+
+@pytest.mark.parametrize("hq,hkv,d,p,dtype", [
+    (8, 8, 64, 16, wl.F32),      # no grouping
+    (8, 1, 64, 16, wl.BF16),     # group 8, eight heads per item
+    (32, 4, 128, 16, wl.BF16),   # group 8, two items of four heads
+    (10, 2, 128, 16, wl.BF16),   # group 5, one head per item
+    (12, 2, 64, 16, wl.F32),     # group 6, two heads per item
+    (4, 2, 128, 1, wl.BF16),     # one token per page
+    (4, 2, 128, 3, wl.F32),      # page size not a power of two
+    (4, 1, 64, 64, wl.BF16),     # large pages
+    (2, 1, 128, 128, wl.F32),    # pages longer than a chunk's stage
+])
+def test_decode_shapes(hq, hkv, d, p, dtype):
+    rng = np.random.default_rng(hq * 1000 + p)
+    kv = rng.integers(1, 1500, size=7)
+    kv[0], kv[1] = 1, 513
+    case = wl.make_attn_case(int(hq + d + p), [1] * 7, kv, hq, hkv, d, p, dtype,
+                             num_pages=int(np.sum(-(-kv // p))) + 5)
+    check(case)
+
+
+def test_decode_empty_and_single_key_requests():
+    case = wl.make_attn_case(102, [1] * 4, [0, 1, 0, 33], 4, 2, 128, 16, wl.BF16, num_pages=8)
+    o, lse = run_decode(case)
+    o_ref, lse_ref = oracle.attention_case(case)
+    compare(o, lse, o_ref, lse_ref, case.dtype)
+    assert torch.all(o[0] == 0) and torch.all(torch.isneginf(lse[0]))
+
+
+def test_decode_custom_scale_and_long_context():
+    case = wl.make_attn_case(103, [1, 1], [16384, 5000], 8, 2, 128, 16, wl.BF16, sm_scale=0.05)
+    check(case)
+
+
+def test_decode_bad_page_id_is_reported_not_faulted():
+    case = wl.make_attn_case(104, [1, 1], [40, 40], 4, 2, 64, 16, wl.F32, num_pages=6)
+    case.table.page_indices[1] = 1000          # out of range for request 0
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, lse = run_decode(case, status=status)
+    assert int(status.item()) == 3
+    # request 1 is unaffected
+    first = int(case.table.page_indptr[1])
+    o_ref, lse_ref = oracle.attention([0, 1], case.kv_len[1:], [0, int(case.table.page_indptr[2]) - first],
+                                      case.table.page_indices[first:], case.q[1:], case.k_pool, case.v_pool, 4, 2,
+                                      case.scale)
+    np.testing.assert_allclose(o[1].cpu().numpy(), o_ref[0], atol=1e-4)
+
+
+def test_decode_length_above_bound_is_reported():
+    case = wl.make_attn_case(105, [1, 1], [40, 20], 4, 2, 64, 16, wl.F32, num_pages=6)
+    d = DevCase(case)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pd.pd_attn_decode(d.q, d.k_pool, d.v_pool, d.kv_len, d.page_indptr, d.page_indices, max_kv_len=30,
+                      dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 2
+
+
+def test_decode_is_deterministic():
+    case = wl.make_attn_case(106, [1] * 9, [900] * 9, 32, 8, 128, 16, wl.BF16)
+    a, la = run_decode(case)
+    b, lb = run_decode(case)
+    assert torch.equal(a, b) and torch.equal(la, lb)

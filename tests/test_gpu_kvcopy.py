@@ -1,0 +1,139 @@
+"""GPU parity of pd_kv_append / pd_kv_pack / pd_kv_unpack against the oracle:
+bit-exact on every logical slot; slots that hold no token stay untouched."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import decode_ragged_paged_gb300 as pd
+    from gpu_util import DevCase, dev_tensor
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    if t.dtype == torch.float32:
+        return t.view(torch.int32).cpu().numpy().view(np.uint32)
+    return t.cpu().numpy()
+
+
+def _host_bits(a: np.ndarray) -> np.ndarray:
+    return a.view(np.uint16) if a.dtype == np.uint16 else a.view(np.uint32)
+
+
+@pytest.mark.parametrize("args", [
+    dict(seed=201, qo=[5, 1, 16, 33], kv=[9, 30, 16, 40], hkv=4, d=128, p=16, dt=wl.BF16),
+    dict(seed=202, qo=[3, 7], kv=[3, 11], hkv=2, d=64, p=1, dt=wl.F32),
+    dict(seed=203, qo=[20, 1, 1], kv=[70, 64, 65], hkv=3, d=64, p=64, dt=wl.BF16),
+])
+def test_append_small(args):
+    case = wl.make_attn_case(args["seed"], args["qo"], args["kv"], args["hkv"], args["hkv"], args["d"], args["p"],
+                             args["dt"], with_new_tokens=True, num_pages=40)
+    d = DevCase(case)
+    pd.pd_kv_append(d.k_new, d.v_new, d.k_pool, d.v_pool, d.qo_indptr, d.kv_len, d.page_indptr, d.page_indices,
+                    max_kv_len=d.max_kv_len)
+    k, v = case.k_pool.copy(), case.v_pool.copy()
+    oracle.kv_append(case.qo_indptr, case.kv_len, case.table.page_indptr, case.table.page_indices,
+                     case.k_new, case.v_new, k, v)
+    np.testing.assert_array_equal(_bits(d.k_pool), _host_bits(k))
+    np.testing.assert_array_equal(_bits(d.v_pool), _host_bits(v))
+
+
+def test_append_causal_prefill_workload_full():
+    # 8 x 512 new tokens, 40 kv heads, D 128, page 16, bf16 -> 256 pages
+    case = wl.causal_prefill()
+    d = DevCase(case)
+    pd.pd_kv_append(d.k_new, d.v_new, d.k_pool, d.v_pool, d.qo_indptr, d.kv_len, d.page_indptr, d.page_indices,
+                    max_kv_len=512)
+    k, v = case.k_pool.copy(), case.v_pool.copy()
+    oracle.kv_append(case.qo_indptr, case.kv_len, case.table.page_indptr, case.table.page_indices,
+                     case.k_new, case.v_new, k, v)
+    np.testing.assert_array_equal(_bits(d.k_pool), _host_bits(k))
+    np.testing.assert_array_equal(_bits(d.v_pool), _host_bits(v))
+
+
+def _handoff_roundtrip(hc: wl.HandoffCase, check_oracle_layers=None):
+    es = wl.element_size(hc.dtype)
+    L, H, D = hc.num_layers, hc.num_kv_heads, hc.head_dim
+    k_src, v_src = dev_tensor(hc.k_src), dev_tensor(hc.v_src)
+    kv_len = dev_tensor(hc.kv_len.astype(np.int32))
+    s_ptr, s_idx = dev_tensor(hc.src_table.page_indptr), dev_tensor(hc.src_table.page_indices)
+    d_ptr, d_idx = dev_tensor(hc.dst_table.page_indptr), dev_tensor(hc.dst_table.page_indices)
+    offs = dev_tensor(hc.dst_offsets)
+    total = wl.packed_bytes(hc.kv_len, L, H, D, es)
+    buf = torch.empty(total, dtype=torch.uint8, device="cuda")
+    max_kv = int(hc.kv_len.max())
+    pd.pd_kv_pack(k_src, v_src, kv_len, s_ptr, s_idx, buf, offs, max_kv_len=max_kv)
+    shape = (L, hc.dst_table.num_pages, H, hc.dst_page_size, D)
+    poison = wl._poison(shape, hc.dtype)
+    k_dst, v_dst = dev_tensor(poison), dev_tensor(poison)
+    pd.pd_kv_unpack(buf, offs, k_dst, v_dst, kv_len, d_ptr, d_idx, max_kv_len=max_kv)
+    again = torch.empty_like(buf)
+    pd.pd_kv_pack(k_dst, v_dst, kv_len, d_ptr, d_idx, again, offs, max_kv_len=max_kv)
+    torch.cuda.synchronize()
+    assert torch.equal(buf, again), "pack(unpack(pack(x))) != pack(x)"
+    return buf, k_dst, v_dst
+
+
+def test_pack_unpack_small_against_oracle():
+    hc = wl.kv_handoff(seed=204, batch=3, layers=3, heads=4, head_dim=64, src_page=16, dst_page=64,
+                       dtype=wl.BF16, kv_lens=[100, 17, 64], src_slack=5, dst_slack=2)
+    buf, k_dst, v_dst = _handoff_roundtrip(hc)
+    total = buf.numel()
+    ref = oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, hc.k_src, hc.v_src,
+                         hc.dst_offsets, total)
+    np.testing.assert_array_equal(buf.cpu().numpy(), ref)
+    shape = (3, hc.dst_table.num_pages, 4, 64, 64)
+    k_ref, v_ref = wl._poison(shape, hc.dtype), wl._poison(shape, hc.dtype)
+    oracle.kv_unpack(hc.kv_len, hc.dst_table.page_indptr, hc.dst_table.page_indices, ref, hc.dst_offsets,
+                     k_ref, v_ref)
+    np.testing.assert_array_equal(_bits(k_dst), _host_bits(k_ref))
+    np.testing.assert_array_equal(_bits(v_dst), _host_bits(v_ref))
+
+
+def test_pack_unpack_fp32_odd_pages():
+    hc = wl.kv_handoff(seed=205, batch=2, layers=2, heads=2, head_dim=64, src_page=3, dst_page=5,
+                       dtype=wl.F32, kv_lens=[13, 1])
+    buf, k_dst, v_dst = _handoff_roundtrip(hc)
+    ref = oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, hc.k_src, hc.v_src,
+                         hc.dst_offsets, buf.numel())
+    np.testing.assert_array_equal(buf.cpu().numpy(), ref)
+
+
+def test_handoff_workload_full_sampled():
+    # 8 requests x 512 tokens x 40 layers x 40 heads x 128, bf16; pages 16 -> 64.
+    # The full round trip is checked on the GPU (pack o unpack o pack); layers
+    # 0, 17 and 39 of every request are checked against the oracle.
+    hc = wl.kv_handoff()
+    buf, k_dst, v_dst = _handoff_roundtrip(hc)
+    layers = [0, 17, 39]
+    sub = wl.HandoffCase(hc.dtype, len(layers), hc.num_kv_heads, hc.head_dim, hc.kv_len, hc.src_page_size,
+                         hc.src_table, np.ascontiguousarray(hc.k_src[layers]), np.ascontiguousarray(hc.v_src[layers]),
+                         hc.dst_page_size, hc.dst_table, None)
+    per = 2 * hc.num_kv_heads * 512 * hc.head_dim * 2  # bytes of one layer of one request
+    sub_offs = np.arange(8, dtype=np.int64) * per * len(layers)
+    ref = oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, sub.k_src, sub.v_src,
+                         sub_offs, per * len(layers) * 8)
+    host = buf.cpu().numpy()
+    for r in range(8):
+        for j, layer in enumerate(layers):
+            got = host[hc.dst_offsets[r] + layer * per: hc.dst_offsets[r] + (layer + 1) * per]
+            exp = ref[sub_offs[r] + j * per: sub_offs[r] + (j + 1) * per]
+            np.testing.assert_array_equal(got, exp)
+
+
+def test_pack_bad_offset_is_reported():
+    hc = wl.kv_handoff(seed=206, batch=2, layers=1, heads=2, head_dim=64, src_page=16, dst_page=16,
+                       dtype=wl.BF16, kv_lens=[16, 16])
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    buf = torch.zeros(4 * 16 * 64 * 2 * 2 + 64, dtype=torch.uint8, device="cuda")
+    offs = dev_tensor(np.array([0, 8], dtype=np.int64))
+    pd.pd_kv_pack(dev_tensor(hc.k_src), dev_tensor(hc.v_src), dev_tensor(hc.kv_len), dev_tensor(hc.src_table.page_indptr),
+                  dev_tensor(hc.src_table.page_indices), buf, offs, max_kv_len=16, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 6

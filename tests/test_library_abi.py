@@ -1,0 +1,105 @@
+"""CPU checks of the C ABI: the library builds, loads and exports every
+symbol that include/pd.h declares; host-side argument checks reject bad input
+without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import decode_ragged_paged_gb300 as pd
+from decode_ragged_paged_gb300 import build as pdbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "pd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pd_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pdbuild.build()
+    return pd.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(pd.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    assert lib.pd_version() >= 100
+    for code in (0, -1, -2, -3, -4):
+        assert lib.pd_status_string(code)
+    for code in range(7):
+        assert lib.pd_device_status_string(code) != b"unknown device status"
+
+
+def _desc(**kw):
+    d = dict(num_qo_heads=8, num_kv_heads=2, head_dim=128, page_size=16, kv_dtype=pd.PD_BF16,
+             o_dtype=pd.PD_BF16, layout=0, causal=1, sm_scale=0.0)
+    d.update(kw)
+    return pd.AttnDesc(**d)
+
+
+def _batch(**kw):
+    fake = 0x1000  # never dereferenced: every call below fails host checks first
+    b = dict(batch_size=2, qo_indptr=fake, kv_len=fake, page_indptr=fake, page_indices=fake, num_pages=4,
+             total_qo=2, max_qo_len=1, max_kv_len=32)
+    b.update(kw)
+    return pd.Batch(**b)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_kv_heads=3), pd.PD_ERR_INVALID_ARG),
+    (dict(head_dim=96), pd.PD_ERR_UNSUPPORTED),
+    (dict(page_size=0), pd.PD_ERR_INVALID_ARG),
+    (dict(kv_dtype=7), pd.PD_ERR_INVALID_ARG),
+    (dict(layout=1), pd.PD_ERR_UNSUPPORTED),
+])
+def test_decode_rejects_bad_descriptor(lib, kw, code):
+    rc = lib.pd_attn_decode(ctypes.byref(_desc(**kw)), ctypes.byref(_batch()), 16, 16, 16, 16, None, 16, 1 << 30,
+                            None, None)
+    assert rc == code
+
+
+def test_decode_rejects_bad_batch_and_pointers(lib):
+    d = _desc()
+    assert lib.pd_attn_decode(ctypes.byref(d), ctypes.byref(_batch(num_pages=0)), 16, 16, 16, 16, None, 16,
+                              1 << 30, None, None) == pd.PD_ERR_INVALID_ARG
+    assert lib.pd_attn_decode(ctypes.byref(d), ctypes.byref(_batch(kv_len=None)), 16, 16, 16, 16, None, 16,
+                              1 << 30, None, None) == pd.PD_ERR_INVALID_ARG
+    # misaligned q
+    assert lib.pd_attn_decode(ctypes.byref(d), ctypes.byref(_batch()), 18, 16, 16, 16, None, 16, 1 << 30,
+                              None, None) == pd.PD_ERR_INVALID_ARG
+    # workspace too small
+    assert lib.pd_attn_decode(ctypes.byref(d), ctypes.byref(_batch()), 16, 16, 16, 16, None, 16, 8,
+                              None, None) == pd.PD_ERR_WORKSPACE
+    # empty batch is a no-op
+    assert lib.pd_attn_decode(ctypes.byref(d), ctypes.byref(_batch(batch_size=0)), None, None, None, None,
+                              None, None, 0, None, None) == pd.PD_OK
+
+
+def test_workspace_size_query(lib):
+    n = lib.pd_attn_workspace_size(ctypes.byref(_desc()), ctypes.byref(_batch()), pd.PD_KIND_DECODE)
+    assert n > 0 and n % 256 == 0
+    assert lib.pd_attn_workspace_size(ctypes.byref(_desc(num_kv_heads=3)), ctypes.byref(_batch()), 0) == 0
+
+
+def test_kv_copies_reject_bad_descriptor(lib):
+    b = _batch()
+    bad = [pd.KvDesc(0, 128, 16, pd.PD_BF16, 0, 1, 0),            # no heads
+           pd.KvDesc(2, 4, 16, pd.PD_BF16, 0, 1, 0),              # 8-byte rows
+           pd.KvDesc(2, 128, 16, pd.PD_BF16, 0, 2, 8),            # unaligned layer stride
+           pd.KvDesc(2, 128, 16, pd.PD_BF16, 1, 1, 0)]            # NHD not built
+    for d in bad:
+        assert lib.pd_kv_pack(ctypes.byref(d), ctypes.byref(b), 16, 16, 16, 1 << 20, 16, None, None) < 0
+        assert lib.pd_kv_unpack(ctypes.byref(d), ctypes.byref(b), 16, 1 << 20, 16, 16, 16, None, None) < 0
+    two_layers = pd.KvDesc(2, 128, 16, pd.PD_BF16, 0, 2, 1 << 20)
+    assert lib.pd_kv_append(ctypes.byref(two_layers), ctypes.byref(b), 16, 16, 16, 16, None, None) == \
+        pd.PD_ERR_INVALID_ARG
