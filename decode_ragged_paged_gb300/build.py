@@ -56,9 +56,18 @@ def _compile(src: str, verbose_ptxas: bool) -> tuple[str, str]:
     return obj, r.stderr
 
 
+def _host_stamp() -> str:
+    import platform
+    return f"{platform.machine()} {nvcc()}"
+
+
 def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:
     """Compile every kernel and the C ABI into libpd.so; returns its path."""
     os.makedirs(OBJ, exist_ok=True)
+    stamp = os.path.join(OBJ, "host.txt")
+    # objects and the library built on another host (another CPU architecture) are never reused
+    if not os.path.exists(stamp) or open(stamp).read() != _host_stamp() or not os.path.exists(LIB):
+        force = True
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     deps = _deps()
     todo = [s for s in sources
@@ -76,6 +85,8 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
         os.replace(tmp, LIB)
+    with open(stamp, "w") as f:
+        f.write(_host_stamp())
     if verbose_ptxas:
         sys.stderr.write("".join(logs))
     return LIB

@@ -38,13 +38,18 @@ def lib_path(mutant: int = 0) -> str:
 def build(mutant: int = 0, force: bool = False) -> str:
     """Compile the oracle (gcc, fp64, OpenMP). Returns the shared-object path."""
     out = lib_path(mutant)
-    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+    import platform
+    stamp = out + ".host"
+    same_host = os.path.exists(stamp) and open(stamp).read() == platform.machine()
+    if not force and same_host and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
         return out
     tmp = out + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
            f"-DORACLE_MUTANT={int(mutant)}", _SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
+    with open(stamp, "w") as f:
+        f.write(platform.machine())
     return out
 
 
