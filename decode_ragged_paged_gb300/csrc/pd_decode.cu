@@ -26,11 +26,37 @@ namespace pd {
 
 namespace {
 
-constexpr int kTS = 16;              // tokens per ring stage
-constexpr int kNC = 4;               // consumer warps
+// Tuning knobs (compile-time). Measured on GB300 for the 128-request GQA
+// decode: a TMA bulk copy stream is limited per issuing warp (a warp keeps only
+// a few copies in flight), so bandwidth comes from many small CTAs, each with
+// its own producer warp: 2 consumer warps, 32-token stages, a 32 KiB ring and
+// 5 CTAs per SM.
+#ifndef PD_DECODE_STAGE_TOKENS
+#define PD_DECODE_STAGE_TOKENS 32
+#endif
+#ifndef PD_DECODE_WARPS
+#define PD_DECODE_WARPS 2
+#endif
+#ifndef PD_DECODE_RING_KB
+#define PD_DECODE_RING_KB 32
+#endif
+#ifndef PD_DECODE_MIN_BLOCKS
+#define PD_DECODE_MIN_BLOCKS 5
+#endif
+// Producer lanes: lane j of the producer warp issues the stages whose running
+// index is j modulo this count.
+#ifndef PD_DECODE_PRODUCER_LANES
+#define PD_DECODE_PRODUCER_LANES 1
+#endif
+constexpr int kTS = PD_DECODE_STAGE_TOKENS;  // tokens per ring stage
+constexpr int kTPL = kTS / 4;                 // tokens per lane per stage (4 token groups per warp)
+constexpr int kNC = PD_DECODE_WARPS;          // consumer warps
+constexpr int kPL = PD_DECODE_PRODUCER_LANES;  // issuing lanes of the producer warp
 constexpr int kThreads = (kNC + 1) * 32;
-constexpr int kMaxChunk = 512;       // longest chunk (tokens) a work item covers
-constexpr int kRingBytes = 64 * 1024;
+static_assert(kPL >= 1 && kPL <= 32, "producer lanes");
+constexpr int kMaxChunk = 512;                // longest chunk (tokens) a work item covers
+constexpr int kRingBytes = PD_DECODE_RING_KB * 1024;
+static_assert(kTS % 4 == 0 && kMaxChunk % kTS == 0, "stage size");
 constexpr unsigned kFull = 0xffffffffu;
 
 template <int ES, int D>
@@ -41,8 +67,15 @@ struct Geo {
   static constexpr int kEpv = 16 / ES;                // elements per vector
   static constexpr int kE = kVecPerLane * kEpv;       // elements per lane = D / 8
   static constexpr int kStageBytes = kTS * kRowBytes;
-  static constexpr int kStages = kRingBytes / kStageBytes < 16 ? kRingBytes / kStageBytes : 16;
+  static constexpr int kStages = kRingBytes / kStageBytes < 32 ? kRingBytes / kStageBytes : 32;
   static_assert(kVecPerLane >= 1, "row too short");
+  // Within a K or V phase stage s belongs to consumer warp s % kNC and uses ring
+  // slot (running index) % kStages. With kStages a multiple of kNC every use of
+  // a slot inside one phase belongs to the same warp, so a warp never waits on a
+  // slot whose previous use (another warp's stage) is still in flight: an
+  // mbarrier parity wait cannot tell a phase two steps back from the pending
+  // one. Phases and items are separated by all-consumer syncs.
+  static_assert(kStages >= kNC && kStages % kNC == 0, "ring stages must be a multiple of the consumer warps");
 };
 
 template <int GS, int D>
@@ -83,6 +116,17 @@ __device__ __forceinline__ void load_lane_row(const uint8_t* row, int dg, float 
       f[vi * 4 + 3] = __uint_as_float(x.w);
     }
   }
+}
+
+// d = a * b + c on a pair of fp32 values with one packed instruction.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
 }
 
 template <int ES, int D>
@@ -221,7 +265,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
 
 // ----------------------------------------------------------------- decode
 template <int ES, int D, int GS>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, PD_DECODE_MIN_BLOCKS) decode_kernel(const DecodeParams p) {
   using G = Geo<ES, D>;
   constexpr int E = G::kE;
   constexpr int NS = G::kStages;
@@ -256,61 +300,49 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
 
   if (warp == kNC) {
     // ---------------------------------------------------------- producer
-    const uint64_t policy = make_evict_first();
+    // Lanes 0..kPL-1 are independent producers: each walks the same item and
+    // stage sequence and issues the stages that fall to it (one bulk copy per
+    // contiguous page run of the HND layout).
     uint32_t ctr = 0;
-    const uint8_t* kpool = static_cast<const uint8_t*>(p.k_pool);
-    const uint8_t* vpool = static_cast<const uint8_t*>(p.v_pool);
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-      const Item I = decode_item(p, it);
-      if (I.q_row < 0) continue;
-      const int32_t* pages = p.page_indices + p.page_indptr[I.r];
-      const int first_page = I.t_begin / p.page_size;
-      const int last_page = (I.t_end - 1) / p.page_size;
-      for (int kv = 0; kv < 2; ++kv) {
-        const uint8_t* pool = kv ? vpool : kpool;
-        int win_base = -(1 << 30);
-        int32_t win_pid = 0;
-        for (int t0 = I.t_begin; t0 < I.t_end; t0 += kTS, ++ctr) {
-          const int slot = ctr % NS;
-          const uint32_t ph = (ctr / NS) & 1u;
-          if (!mbar_wait(&empty[slot], ph ^ 1u, abort, p.status)) goto producer_done;
-          const int t1 = min(t0 + kTS, I.t_end);
-          if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)((t1 - t0) * RB));
-          int t = t0;
-          while (t < t1) {
-            const int lp = t / p.page_size - first_page;
-            if (lp < win_base || lp >= win_base + 32) {
-              win_base = lp;
-              const int k = first_page + lp + lane;
-              int32_t pid = 0;
-              if (k <= last_page) {
-                pid = __ldg(pages + k);
-                if (pid < 0 || pid >= p.num_pages) {
-                  report(p.status, PD_DEV_BAD_PAGE_TABLE);
-                  pid = 0;
-                }
+    if (lane < kPL) {
+      const uint64_t policy = make_evict_first();
+      const uint8_t* kpool = static_cast<const uint8_t*>(p.k_pool);
+      const uint8_t* vpool = static_cast<const uint8_t*>(p.v_pool);
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const Item I = decode_item(p, it);
+        if (I.q_row < 0) continue;
+        const int32_t* pages = p.page_indices + p.page_indptr[I.r];
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint8_t* pool = kv ? vpool : kpool;
+          for (int t0 = I.t_begin; t0 < I.t_end; t0 += kTS, ++ctr) {
+            if ((int)(ctr % kPL) != lane) continue;
+            const int slot = ctr % NS;
+            if (!mbar_wait(&empty[slot], ((ctr / NS) & 1u) ^ 1u, abort, p.status)) goto producer_done;
+            const int t1 = min(t0 + kTS, I.t_end);
+            mbar_arrive_expect_tx(&full[slot], (uint32_t)((t1 - t0) * RB));
+            for (int t = t0; t < t1;) {
+              const int slot_in_page = t % p.page_size;
+              const int run = min(t1 - t, p.page_size - slot_in_page);
+              int32_t pid = __ldg(pages + t / p.page_size);
+              if (pid < 0 || pid >= p.num_pages) {
+                report(p.status, PD_DEV_BAD_PAGE_TABLE);
+                pid = 0;
               }
-              win_pid = pid;
+              const uint8_t* src = pool + (((int64_t)pid * p.hkv + I.g) * p.page_size + slot_in_page) * (int64_t)RB;
+              bulk_g2s_hint(ring + (size_t)slot * SB + (size_t)(t - t0) * RB, src, (uint32_t)(run * RB), &full[slot],
+                            policy);
+              t += run;
             }
-            const int32_t pid = __shfl_sync(kFull, win_pid, lp - win_base);
-            const int slot_in_page = t % p.page_size;
-            const int run = min(t1 - t, p.page_size - slot_in_page);
-            if (lane == 0) {
-              const uint8_t* src =
-                  pool + (((int64_t)pid * p.hkv + I.g) * p.page_size + slot_in_page) * (int64_t)RB;
-              bulk_g2s_hint(ring + (size_t)slot * SB + (size_t)(t - t0) * RB, src, (uint32_t)(run * RB),
-                            &full[slot], policy);
-            }
-            t += run;
           }
         }
       }
     }
   producer_done:
-    // On an abort, give the copies still in flight a bounded chance to land
-    // before the CTA's shared memory is released.
-    if (*abort && lane == 0) {
+    // On an abort, give this lane's copies still in flight a bounded chance to
+    // land before the CTA's shared memory is released.
+    if (*abort && lane < kPL) {
       for (uint32_t k = (ctr > (uint32_t)NS ? ctr - NS : 0); k < ctr; ++k) {
+        if ((int)(k % kPL) != lane) continue;
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(&full[k % NS], (k / NS) & 1u) && globaltimer_ns() - t0 < kWaitLimitNs) {
         }
@@ -345,23 +377,24 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         const int slot = ctr % NS;
         if (!mbar_wait(&full[slot], (ctr / NS) & 1u, abort, p.status)) goto consumer_done;
         const uint8_t* buf = ring + (size_t)slot * SB;
-        float acc[4 * GS];
+        float acc[kTPL * GS];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < kTPL; ++i) {
           float kf[E];
           load_lane_row<ES, D>(buf + (size_t)(tg + 4 * i) * RB, dg, kf);
 #pragma unroll
           for (int h = 0; h < GS; ++h) {
-            float a = 0.f;
+            float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < E; ++e) a = fmaf(qr[h][e], kf[e], a);
-            acc[i * GS + h] = a;
+            for (int e = 0; e < E; e += 2)
+              a = ffma2(make_float2(qr[h][e], qr[h][e + 1]), make_float2(kf[e], kf[e + 1]), a);
+            acc[i * GS + h] = a.x + a.y;
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
-        xreduce<4 * GS, 4>(acc, lane);
-        constexpr int N = 4 * GS;
+        xreduce<kTPL * GS, 4>(acc, lane);
+        constexpr int N = kTPL * GS;
         constexpr int CNT = N >= 8 ? N / 8 : 1;
         constexpr int SHIFT = N >= 8 ? 0 : (N == 4 ? 1 : 2);
         const bool writer = N >= 8 ? true : ((dg & ((1 << SHIFT) - 1)) == 0);
@@ -401,11 +434,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
       if (!consumer_sync(sync_bar, sync_phase, lane, abort, p.status)) goto consumer_done;
 
       // ---- V phase: weighted sum of this warp's stages
-      float oacc[GS][E];
+      float2 oacc[GS][E / 2];
 #pragma unroll
       for (int h = 0; h < GS; ++h)
 #pragma unroll
-        for (int e = 0; e < E; ++e) oacc[h][e] = 0.f;
+        for (int e = 0; e < E / 2; ++e) oacc[h][e] = make_float2(0.f, 0.f);
       for (int s = 0; s < n_st; ++s, ++ctr) {
         if ((s % kNC) != cw) continue;
         const int slot = ctr % NS;
@@ -413,7 +446,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         const uint8_t* buf = ring + (size_t)slot * SB;
         const int valid = min(kTS, n_tok - s * kTS);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < kTPL; ++i) {
           const int j = tg + 4 * i;
           if (j < valid) {
             float pw[GS];
@@ -424,7 +457,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
 #pragma unroll
             for (int h = 0; h < GS; ++h)
 #pragma unroll
-              for (int e = 0; e < E; ++e) oacc[h][e] = fmaf(pw[h], vf[e], oacc[h][e]);
+              for (int e = 0; e < E / 2; ++e)
+                oacc[h][e] = ffma2(make_float2(pw[h], pw[h]), make_float2(vf[2 * e], vf[2 * e + 1]), oacc[h][e]);
           }
         }
         __syncwarp();
@@ -434,17 +468,22 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
 #pragma unroll
       for (int h = 0; h < GS; ++h)
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          float v = oacc[h][e];
-          v += __shfl_xor_sync(kFull, v, 8);
-          v += __shfl_xor_sync(kFull, v, 16);
+        for (int e = 0; e < E / 2; ++e) {
+          float2 v = oacc[h][e];
+          v.x += __shfl_xor_sync(kFull, v.x, 8);
+          v.y += __shfl_xor_sync(kFull, v.y, 8);
+          v.x += __shfl_xor_sync(kFull, v.x, 16);
+          v.y += __shfl_xor_sync(kFull, v.y, 16);
           oacc[h][e] = v;
         }
       if (tg == 0) {
 #pragma unroll
         for (int h = 0; h < GS; ++h)
 #pragma unroll
-          for (int e = 0; e < E; ++e) s_opart[(cw * GS + h) * D + lane_dim<ES, D>(dg, e)] = oacc[h][e];
+          for (int e = 0; e < E / 2; ++e) {
+            s_opart[(cw * GS + h) * D + lane_dim<ES, D>(dg, 2 * e)] = oacc[h][e].x;
+            s_opart[(cw * GS + h) * D + lane_dim<ES, D>(dg, 2 * e + 1)] = oacc[h][e].y;
+          }
       }
       if (!consumer_sync(sync_bar, sync_phase, lane, abort, p.status)) goto consumer_done;
 

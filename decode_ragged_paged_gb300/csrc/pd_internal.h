@@ -2,6 +2,7 @@
 // the C-ABI layer (pd_api.cu) and the kernel translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -79,6 +80,12 @@ struct KvCopyParams {
 int launch_kv_append(const KvCopyParams& p, cudaStream_t stream);
 int launch_kv_pack(const KvCopyParams& p, cudaStream_t stream);
 int launch_kv_unpack(const KvCopyParams& p, cudaStream_t stream);
+
+// ------------------------------------------------------------ tensor maps
+bool make_pool_map(CUtensorMap* map, const void* pool, int32_t dtype, int32_t num_pages, int32_t hkv,
+                   int32_t page_size, int32_t head_dim, int32_t box_cols, int32_t box_rows, bool swizzle128);
+bool make_rows_map(CUtensorMap* map, const void* base, int32_t dtype, int32_t total, int32_t hq, int32_t head_dim,
+                   int32_t box_cols, int32_t box_rows, bool swizzle128);
 
 // ------------------------------------------------------------------- misc
 int device_sm_count();

@@ -1,0 +1,73 @@
+// pd_tmap.cu -- host-side construction of TMA tensor maps (CUtensorMap) for the
+// query rows and the HND page pools. The driver entry point is looked up once
+// through the runtime, so the library links only against libcudart.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "pd_internal.h"
+
+namespace pd {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+CUtensorMapDataType tma_dtype(int32_t dtype) {
+  return dtype == PD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+}
+
+}  // namespace
+
+// Pool [num_pages][hkv][page_size][head_dim] as a 4-D tensor {head_dim, page_size,
+// hkv, num_pages} (innermost first); one box = box_rows slots x box_cols elements
+// of one (page, head).
+bool make_pool_map(CUtensorMap* map, const void* pool, int32_t dtype, int32_t num_pages, int32_t hkv,
+                   int32_t page_size, int32_t head_dim, int32_t box_cols, int32_t box_rows, bool swizzle128) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const int es = dtype == PD_BF16 ? 2 : 4;
+  cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)page_size, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+  cuuint64_t strides[3] = {(cuuint64_t)head_dim * es, (cuuint64_t)page_size * head_dim * es,
+                           (cuuint64_t)hkv * page_size * head_dim * es};
+  cuuint32_t box[4] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, tma_dtype(dtype), 4, const_cast<void*>(pool), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// q / o rows [total][hq][head_dim] as a 3-D tensor {head_dim, hq, total}; one box
+// = box_rows consecutive rows of one head, box_cols elements wide.
+bool make_rows_map(CUtensorMap* map, const void* base, int32_t dtype, int32_t total, int32_t hq, int32_t head_dim,
+                   int32_t box_cols, int32_t box_rows, bool swizzle128) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const int es = dtype == PD_BF16 ? 2 : 4;
+  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)hq, (cuuint64_t)total};
+  cuuint64_t strides[2] = {(cuuint64_t)head_dim * es, (cuuint64_t)hq * head_dim * es};
+  cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, tma_dtype(dtype), 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace pd
