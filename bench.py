@@ -1,0 +1,450 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-attention / KV-handoff hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline (one JSON line on rank 0): decode attention HBM throughput of the
+decode-batch workload (128 requests, qo_len 1, kv_len U[512, 4096], GQA 32/8,
+head_dim 128, page 16, bf16). A step is one pd_attn_decode call over the batch
+(plan, split-KV decode, merge). `value` = algorithmic bytes (K/V of every
+cached token, q, o, lse and the page table) of all ranks / slowest rank's
+device time. The KV pools (1.14 GB) exceed the 126 MB L2, so no flush is
+needed between steps. `roofline` reports the split-KV decode kernel alone
+(CUDA events around its launch), `e2e` the same metric through the C ABI with
+the step's inputs copied from pinned host memory and its outputs read back
+every step, `rows` the other hot-path steps (append, causal prefill, mixed
+1P63D batch, KV pack and unpack) each against its own roofline, and
+`cpu_baseline` the fp64 oracle on the host cores for a bounded sample.
+
+Under torchrun (N > 1) every rank runs an independent replica (the method has
+no exchange step on one node's attention path): scaling is weak.
+
+--impl reference times the fp64 CPU oracle on the same workload, metric and
+unit, each step a bounded sample; under torchrun rank 0 alone runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "paged-attn decode HBM GB/s; prefill TFLOP/s; KV pack GB/s (% of roofline)"
+WORKLOAD = ("decode batch: 128 requests, qo_len=1, kv_len uniform in [512,4096], GQA 32 q heads / 8 kv heads, "
+            "head_dim 128, page_size 16, bf16, pages a seeded random permutation of the pool")
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "decode_ragged_paged_gb300", "csrc", "*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    e = d.get(kernel)
+    if not e or e.get("csrc") != csrc_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9 or not f[0].isdigit() or int(f[0]) != self.dev:
+                continue
+            try:
+                sm.append(float(f[1].split()[0]))
+                smax.append(float(f[2].split()[0]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- setup
+def init_dist(backend: str):
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def decode_bytes(w) -> int:
+    kv = int(w["kv_len_host"].sum()) * w["hkv"] * w["d"] * 2 * 2
+    q = w["q"].numel() * 2
+    pages = int((-(-w["kv_len_host"] // w["page"])).sum())
+    return kv + 2 * q + w["q"].shape[0] * w["hq"] * 4 + pages * 4 + len(w["kv_len_host"]) * 12
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+    import decode_ragged_paged_gb300 as pd
+    from workloads import torch_gen
+
+    world, rank, local = init_dist("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pd.load_library()
+    peaks = measured_peaks()
+    stream = torch.cuda.current_stream()
+
+    w = torch_gen.decode_batch(device=dev)
+    o = torch.empty_like(w["q"])
+    lse = torch.empty(w["q"].shape[:2], dtype=torch.float32, device=dev)
+    desc = pd.make_attn_desc(w["q"], w["k_pool"])
+    batch = pd.make_batch(w["kv_len"], w["page_indptr"], w["page_indices"], w["k_pool"].shape[0],
+                          total_qo=w["q"].shape[0], max_kv_len=4096)
+    ws = torch.empty(max(pd.pd_attn_workspace_size(desc, batch, pd.PD_KIND_DECODE), 16), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        pd.pd_attn_decode(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"], w["page_indices"],
+                          max_kv_len=4096, o=o, lse=lse, workspace=ws)
+
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        step()
+    ks = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in ks + ke:
+        e.record()  # materialise the CUDA event handles
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler = ClockSampler(local)
+    sampler.start()
+    torch.cuda.synchronize()
+    t0.record()
+    for k in range(K):
+        pd.pd_profile_events(ks[k], ke[k])
+        step()
+    t1.record()
+    pd.pd_profile_events(None, None)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / K
+    kernel_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ks, ke)]))
+    barrier(world)
+    ms_max = max_over_ranks(ms, world, dev)
+    step_bytes = decode_bytes(w)
+    value = step_bytes * world / (ms_max * 1e-3) / 1e9
+
+    # e2e: inputs from pinned host memory, outputs read back, every step
+    h_q = w["q"].cpu().pin_memory()
+    h_tables = [t.cpu().pin_memory() for t in (w["kv_len"], w["page_indptr"], w["page_indices"])]
+    d_tables = [torch.empty_like(t) for t in (w["kv_len"], w["page_indptr"], w["page_indices"])]
+    d_q = torch.empty_like(w["q"])
+    h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = h_q.numel() * 2 + sum(t.numel() * 4 for t in h_tables)
+    d2h = h_o.numel() * 2 + h_lse.numel() * 4
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        for d, h in zip(d_tables, h_tables):
+            d.copy_(h, non_blocking=True)
+        pd.pd_attn_decode(d_q, w["k_pool"], w["v_pool"], d_tables[0], d_tables[1], d_tables[2], max_kv_len=4096,
+                          o=o, lse=lse, workspace=ws)
+        h_o.copy_(o, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(W):
+        e2e_step()
+    barrier(world)
+    ta = time.perf_counter()
+    for _ in range(K):
+        e2e_step()
+    e2e_ms = (time.perf_counter() - ta) * 1e3 / K
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_value = step_bytes * world / (e2e_ms * 1e-3) / 1e9
+
+    rows = measure_rows(args, dev, peaks) if (rank == 0 and not args.no_rows) else {}
+    clocks = sampler.stop()
+    del w
+
+    if rank != 0:
+        return
+    cpu = cpu_baseline(args) if not args.no_cpu else None
+    achieved = step_bytes / (kernel_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(ms_max, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (1.14 GB of KV pages); no flush between steps",
+                   "step": "one pd_attn_decode call: plan + split-KV decode + merge"},
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
+                     "peak_source": peaks["source"], "traffic": profiled_traffic("decode_kernel"),
+                     "algorithmic_bytes": step_bytes, "kernel_ms": round(kernel_ms, 5)},
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "rows": rows,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def timed(fn, reps, warm, flush=None, prof=True):
+    """Median device time (ms) of fn and of its main kernel (profiling events)."""
+    import torch
+    import decode_ragged_paged_gb300 as pd
+    for _ in range(warm):
+        fn()
+    tot, ker = [], []
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ka, kb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ka.record()
+        kb.record()
+        torch.cuda.synchronize()
+        if prof:
+            pd.pd_profile_events(ka, kb)
+        a.record()
+        fn()
+        b.record()
+        pd.pd_profile_events(None, None)
+        torch.cuda.synchronize()
+        tot.append(a.elapsed_time(b))
+        ker.append(ka.elapsed_time(kb) if prof else tot[-1])
+    return float(np.median(tot)), float(np.median(ker))
+
+
+def measure_rows(args, dev, peaks) -> dict:
+    """The other steps of the hot path, each on its own workload."""
+    import torch
+    import decode_ragged_paged_gb300 as pd
+    from workloads import torch_gen
+
+    rows = {}
+    reps, warm = args.row_reps, 3
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    hbm = peaks["hbm"]
+
+    # causal prefill workload: append of its 4096 new tokens, then attention
+    w = torch_gen.causal_prefill(device=dev)
+    byts = 4 * w["k_new"].numel() * 2
+    ms, kms = timed(lambda: pd.pd_kv_append(w["k_new"], w["v_new"], w["k_pool"], w["v_pool"], w["qo_indptr"],
+                                            w["kv_len"], w["page_indptr"], w["page_indices"], max_kv_len=512),
+                    reps, warm, flush)
+    rows["append"] = {"workload": "8 x 512 new tokens, 40 kv heads, D 128, page 16, bf16", "ms": round(ms, 5),
+                      "GBs": round(byts / kms / 1e6, 1), "frac_hbm": round(byts / kms / 1e6 / hbm, 4),
+                      "bound": "hbm", "bytes": byts}
+    L, H, B = 512, 40, 8
+    flops = 2 * 128 * L * (L + 1) * H * B
+    pf_bytes = 4 * w["q"].numel() * 2
+    try:
+        o = torch.empty_like(w["q"])
+        ms, kms = timed(lambda: pd.pd_attn_prefill(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
+                                                   w["page_indices"], w["qo_indptr"], max_qo_len=512,
+                                                   max_kv_len=512, o=o), reps, warm, flush)
+        t = flops / (kms * 1e-3) / 1e12
+        rows["prefill"] = {"workload": "8 x 512 causal, 40 heads, D 128, page 16, bf16", "ms": round(ms, 5),
+                           "TFLOPs": round(t, 1), "frac_bf16": round(t / peaks["bf16"], 4),
+                           "GBs": round(pf_bytes / kms / 1e6, 1), "frac_hbm": round(pf_bytes / kms / 1e6 / hbm, 4),
+                           "bound": "hbm (128 flop/B < ridge)", "flops": flops, "bytes": pf_bytes}
+    except pd.PdError as e:
+        rows["prefill"] = {"status": str(e)}
+    del w
+
+    w = torch_gen.mixed_1p_nd(device=dev)
+    kvb = int(w["kv_len_host"].sum()) * 40 * 128 * 2 * 2 + 2 * w["q"].numel() * 2
+    try:
+        o = torch.empty_like(w["q"])
+        ms, kms = timed(lambda: pd.pd_attn_mixed(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
+                                                 w["page_indices"], w["qo_indptr"], max_qo_len=1024,
+                                                 max_kv_len=1024, o=o), reps, warm, flush)
+        rows["mixed"] = {"workload": "1 prefill (1024) + 63 decodes (kv U[512,576]), 40 heads, D 128, bf16",
+                         "ms": round(ms, 5), "GBs": round(kvb / kms / 1e6, 1),
+                         "frac_hbm": round(kvb / kms / 1e6 / hbm, 4), "bound": "hbm", "bytes": kvb}
+    except pd.PdError as e:
+        rows["mixed"] = {"status": str(e)}
+    del w
+
+    w = torch_gen.kv_handoff(device=dev)
+    byts = 2 * w["buffer"].numel()
+    ms, kms = timed(lambda: pd.pd_kv_pack(w["k_src"], w["v_src"], w["kv_len"], w["src_indptr"], w["src_indices"],
+                                          w["buffer"], w["offsets"], max_kv_len=512), reps, warm)
+    rows["pack"] = {"workload": "8 req x 512 tok x 40 layers x 40 kv heads x 128, bf16, page 16",
+                    "ms": round(ms, 5), "GBs": round(byts / kms / 1e6, 1), "frac_hbm": round(byts / kms / 1e6 / hbm, 4),
+                    "bound": "hbm", "bytes": byts}
+    ms, kms = timed(lambda: pd.pd_kv_unpack(w["buffer"], w["offsets"], w["k_dst"], w["v_dst"], w["kv_len"],
+                                            w["dst_indptr"], w["dst_indices"], max_kv_len=512), reps, warm)
+    rows["unpack"] = {"workload": "same buffers into a page-64 pool with its own table", "ms": round(ms, 5),
+                      "GBs": round(byts / kms / 1e6, 1), "frac_hbm": round(byts / kms / 1e6 / hbm, 4),
+                      "bound": "hbm", "bytes": byts}
+    del w
+    return rows
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_decode_sample(n_req: int, seed: int):
+    import workloads as wl
+    rng = np.random.default_rng(seed)
+    kv = rng.integers(512, 4097, size=n_req)
+    case = wl.make_attn_case(seed, np.ones(n_req, dtype=np.int64), kv, 32, 8, 128, 16, wl.BF16)
+    return case, int(kv.sum()) * 8 * 128 * 2 * 2
+
+
+def time_oracle(case) -> float:
+    import oracle
+    t = time.perf_counter()
+    oracle.attention_case(case)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(args) -> dict:
+    """The fp64 oracle on the host cores, on a bounded sample of the workload."""
+    import oracle
+    oracle.build()
+    case, byts = oracle_decode_sample(2, 77)
+    t1 = max(time_oracle(case), 1e-3)
+    n = int(np.clip(round(2 * args.cpu_seconds / t1), 2, 128))
+    case, byts = oracle_decode_sample(n, 78)
+    t = time_oracle(case)
+    return {"value": round(byts / t / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} of the 128 decode requests (kv_len U[512,4096], 32/8 heads, D 128, bf16), "
+                      f"fp64, {t:.1f} s", "seconds": round(t, 2)}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    case, byts = oracle_decode_sample(2, 77)
+    t1 = max(time_oracle(case), 1e-3)
+    budget = 150.0 / max(args.steps + args.warmup, 1)       # seconds per step for the whole run
+    n = int(np.clip(round(2 * budget / t1), 1, 128))
+    samples = [oracle_decode_sample(n, 100 + s) for s in range(min(args.steps + args.warmup, 8))]
+    for s in range(args.warmup):
+        time_oracle(samples[s % len(samples)][0])
+    tot_t, tot_b = 0.0, 0
+    for s in range(args.steps):
+        case, byts = samples[s % len(samples)]
+        tot_t += time_oracle(case)
+        tot_b += byts
+    value = tot_b / tot_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": "rank 0 only (CPU)",
+                   "step": f"the fp64 oracle over {n} of the 128 decode requests"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle", "cores": oracle.num_threads(),
+                         "sample": f"{n} requests per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--row-reps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-rows", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -34,7 +34,7 @@ DEVICE_STATUS = {0: "ok", 1: "bad indptr", 2: "bad length", 3: "bad page table",
 
 # Every symbol include/pd.h declares.
 EXPORTS = ("pd_attn_workspace_size", "pd_attn_decode", "pd_attn_prefill", "pd_attn_mixed",
-           "pd_kv_append", "pd_kv_pack", "pd_kv_unpack", "pd_status_string",
+           "pd_kv_append", "pd_kv_pack", "pd_kv_unpack", "pd_profile_events", "pd_status_string",
            "pd_device_status_string", "pd_version")
 
 
@@ -92,6 +92,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.pd_device_status_string.argtypes = [I32]
             lib.pd_device_status_string.restype = ctypes.c_char_p
             lib.pd_version.restype = I32
+            lib.pd_profile_events.argtypes = [P, P]
+            lib.pd_profile_events.restype = ctypes.c_int
             _lib = lib
         return _lib
 
@@ -252,6 +254,14 @@ def pd_kv_unpack(src, src_offsets, k_pools, v_pools, kv_len, page_indptr, page_i
     rc = lib.pd_kv_unpack(ctypes.byref(desc), ctypes.byref(batch), _ptr(src), src.numel() * src.element_size(),
                           _ptr(src_offsets), _ptr(k_pools), _ptr(v_pools), _ptr(dev_status), _stream(stream))
     _check(rc, "pd_kv_unpack")
+
+
+def pd_profile_events(start=None, stop=None) -> None:
+    """Record torch.cuda.Event `start` / `stop` around the main kernel of every
+    following call of this thread (None, None to stop). The events must have
+    been recorded once already so that their CUDA handles exist."""
+    h = (lambda e: None if e is None else e.cuda_event)
+    _check(load_library().pd_profile_events(h(start), h(stop)), "pd_profile_events")
 
 
 def packed_bytes(kv_len_host, num_layers, num_kv_heads, head_dim, elem_size) -> int:

@@ -24,6 +24,11 @@ int device_sm_count() {
   return n;
 }
 
+ProfileEvents& profile_events() {
+  static thread_local ProfileEvents ev;
+  return ev;
+}
+
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -67,6 +72,13 @@ using namespace pd;
 extern "C" {
 
 int32_t pd_version(void) { return 100; }
+
+int pd_profile_events(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr)) return PD_ERR_INVALID_ARG;
+  profile_events().start = static_cast<cudaEvent_t>(start_event);
+  profile_events().stop = static_cast<cudaEvent_t>(stop_event);
+  return PD_OK;
+}
 
 const char* pd_status_string(int32_t code) {
   switch (code) {

@@ -625,7 +625,9 @@ int run_decode(DecodeParams& p, cudaStream_t stream) {
   int64_t grid = (int64_t)device_sm_count() * blocks_per_sm;
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
+  profile_begin(stream);
   decode_kernel<ES, D, GS><<<(unsigned)grid, kThreads, smem, stream>>>(p);
+  profile_end(stream);
   const int warps = p.batch * p.hq;
   if (warps > 0) decode_merge_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;

@@ -90,6 +90,18 @@ bool make_rows_map(CUtensorMap* map, const void* base, int32_t dtype, int32_t to
 // ------------------------------------------------------------------- misc
 int device_sm_count();
 
+// Events of pd_profile_events() (per host thread); recorded around main kernels.
+struct ProfileEvents {
+  cudaEvent_t start = nullptr, stop = nullptr;
+};
+ProfileEvents& profile_events();
+inline void profile_begin(cudaStream_t s) {
+  if (profile_events().start) cudaEventRecord(profile_events().start, s);
+}
+inline void profile_end(cudaStream_t s) {
+  if (profile_events().stop) cudaEventRecord(profile_events().stop, s);
+}
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace pd

@@ -213,19 +213,25 @@ int launch_kv_append(const KvCopyParams& p, cudaStream_t stream) {
   if (p.max_new <= 0 || p.batch <= 0) return PD_OK;
   int grid = copy_grid();
   if (grid > p.max_new) grid = p.max_new;
+  profile_begin(stream);
   kv_append_kernel<<<grid, kCopyThreads, 0, stream>>>(p);
+  profile_end(stream);
   return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
 }
 
 int launch_kv_pack(const KvCopyParams& p, cudaStream_t stream) {
   if (p.batch <= 0 || p.max_kv_len <= 0) return PD_OK;
+  profile_begin(stream);
   kv_pack_kernel<<<copy_grid(), kCopyThreads, 0, stream>>>(p);
+  profile_end(stream);
   return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
 }
 
 int launch_kv_unpack(const KvCopyParams& p, cudaStream_t stream) {
   if (p.batch <= 0 || p.max_kv_len <= 0) return PD_OK;
+  profile_begin(stream);
   kv_unpack_kernel<<<copy_grid(), kCopyThreads, 0, stream>>>(p);
+  profile_end(stream);
   return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
 }
 

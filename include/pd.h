@@ -222,6 +222,17 @@ PD_API int pd_kv_unpack(const pd_kv_desc *desc, const pd_batch *batch, const voi
                         size_t src_bytes, const int64_t *src_offsets, void *k_pool, void *v_pool,
                         int32_t *dev_status, void *stream);
 
+/*
+ * Profiling hook (not part of the method): while set, every call of this host
+ * thread records `start_event` on its stream just before launching its main
+ * kernel (the split-KV decode kernel, the prefill/mixed kernel, the append,
+ * pack or unpack kernel) and `stop_event` just after it, so that
+ * cudaEventElapsedTime gives that kernel's device time alone. Both are
+ * cudaEvent_t handles owned by the caller; pass NULL, NULL to stop. Returns
+ * PD_ERR_INVALID_ARG if exactly one of them is NULL.
+ */
+PD_API int pd_profile_events(void *start_event, void *stop_event);
+
 /* Static description of a pd_status or pd_device_status code (never NULL). */
 PD_API const char *pd_status_string(int32_t code);
 PD_API const char *pd_device_status_string(int32_t code);
