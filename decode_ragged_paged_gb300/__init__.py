@@ -33,7 +33,8 @@ DEVICE_STATUS = {0: "ok", 1: "bad indptr", 2: "bad length", 3: "bad page table",
                  5: "timeout", 6: "bad offset"}
 
 # Every symbol include/pd.h declares.
-EXPORTS = ("pd_attn_workspace_size", "pd_attn_decode", "pd_attn_prefill", "pd_attn_mixed",
+EXPORTS = ("pd_attn_workspace_size", "pd_attn_decode", "pd_attn_decode_static", "pd_attn_prefill",
+           "pd_attn_mixed",
            "pd_kv_append", "pd_kv_pack", "pd_kv_unpack", "pd_profile_events", "pd_status_string",
            "pd_device_status_string", "pd_version")
 

@@ -165,6 +165,27 @@ PD_API int pd_attn_decode(const pd_attn_desc *desc, const pd_batch *batch, const
                    void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * Decode attention without a caller-provided workspace. (The pages have no
+ * counterpart for this call; it exists for callers of this library.)
+ * For callers that cannot allocate device memory for a workspace: for example
+ * a C host program that only receives tensors from a framework owning every
+ * device allocation, or a loop where calling cudaMalloc is not allowed.
+ * Arguments and results are those of pd_attn_decode minus the workspace; the
+ * scratch space is a fixed array of 32 MiB in device memory defined by the
+ * library, reserved on every GPU where it is first used until the process
+ * exits. A batch whose plan and split-KV partials need more than that returns
+ * PD_ERR_WORKSPACE and launches nothing (the 128-request batch with kv_len up to
+ * 4096 and 32 query heads of 128 needs about 17 MiB). All calls on one GPU share
+ * the array: calls whose work overlaps on the GPU (e.g. on two streams) race
+ * and must be serialised by the caller. The first call on each GPU looks up the
+ * array's device address through the CUDA runtime (a one-time step that may load
+ * the library's device code); make that first call outside any stream capture.
+ */
+PD_API int pd_attn_decode_static(const pd_attn_desc *desc, const pd_batch *batch, const void *q,
+                                 const void *k_pool, const void *v_pool, void *o, float *lse,
+                                 int32_t *dev_status, void *stream);
+
+/*
  * Prefill attention: any qo_len <= kv_len per request, causal or not (section
  * "Prefill vs Decode performance": prefill requests bring many tokens and are
  * compute bound). Arguments as pd_attn_decode with q, o [total_qo][Hq][D]
