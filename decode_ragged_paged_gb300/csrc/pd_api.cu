@@ -107,6 +107,7 @@ const char* pd_device_status_string(int32_t code) {
 size_t pd_attn_workspace_size(const pd_attn_desc* desc, const pd_batch* batch, int32_t kind) {
   if (check_attn(desc, batch, false) != PD_OK) return 0;
   if (kind == PD_KIND_DECODE) return decode_layout_for(desc, batch).total;
+  if (kind == PD_KIND_PREFILL) return prefill_layout(batch->batch_size, batch->total_qo, batch->max_qo_len).total;
   return 0;
 }
 
@@ -162,11 +163,42 @@ int pd_attn_decode(const pd_attn_desc* desc, const pd_batch* batch, const void* 
 int pd_attn_prefill(const pd_attn_desc* desc, const pd_batch* batch, const void* q, const void* k_pool,
                     const void* v_pool, void* o, float* lse, void* workspace, size_t workspace_bytes,
                     int32_t* dev_status, void* stream) {
-  (void)q; (void)k_pool; (void)v_pool; (void)o; (void)lse; (void)workspace; (void)workspace_bytes;
-  (void)dev_status; (void)stream;
-  const int rc = check_attn(desc, batch, true);
+  int rc = check_attn(desc, batch, true);
   if (rc != PD_OK) return rc;
-  return PD_ERR_UNSUPPORTED;
+  rc = prefill_supported(desc->kv_dtype, desc->head_dim, desc->page_size);
+  if (rc != PD_OK) return rc;
+  if (batch->batch_size == 0 || batch->total_qo == 0) return PD_OK;
+  if (q == nullptr || k_pool == nullptr || v_pool == nullptr || o == nullptr || workspace == nullptr)
+    return PD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o) || !aligned16(workspace))
+    return PD_ERR_INVALID_ARG;
+  const PrefillLayout L = prefill_layout(batch->batch_size, batch->total_qo, batch->max_qo_len);
+  if (workspace_bytes < L.total) return PD_ERR_WORKSPACE;
+  PrefillParams p{};
+  p.batch = batch->batch_size;
+  p.hq = desc->num_qo_heads;
+  p.hkv = desc->num_kv_heads;
+  p.group = p.hq / p.hkv;
+  p.page_size = desc->page_size;
+  p.num_pages = batch->num_pages;
+  p.total_qo = batch->total_qo;
+  p.max_qo_len = batch->max_qo_len;
+  p.max_kv_len = batch->max_kv_len;
+  p.causal = desc->causal ? 1 : 0;
+  p.o_dtype = desc->o_dtype;
+  p.max_rq = L.max_rq;
+  p.scale_log2 = scale_of(desc) * kLog2e;
+  p.qo_indptr = batch->qo_indptr;
+  p.kv_len = batch->kv_len;
+  p.page_indptr = batch->page_indptr;
+  p.page_indices = batch->page_indices;
+  p.o = o;
+  p.lse = lse;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
+  p.rq_list = reinterpret_cast<int2*>(ws + L.rq_list);
+  p.status = dev_status;
+  return launch_prefill(p, q, k_pool, v_pool, static_cast<cudaStream_t>(stream));
 }
 
 int pd_attn_mixed(const pd_attn_desc* desc, const pd_batch* batch, const void* q, const void* k_pool,

@@ -113,6 +113,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Warp-collective form of mbar_wait: every lane of the warp calls it and all get
+// the same answer, so that a timeout never splits a warp before a warp-wide
+// instruction (shuffles, __syncwarp, tcgen05 .sync.aligned operations).
+__device__ __forceinline__ bool warp_mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               int32_t* status) {
+  const bool ok = mbar_wait(bar, parity, abort, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // -------------------------------------------------------- bulk async copies
 // Global -> shared copy by the TMA engine; completion is counted in bytes on `bar`.
 // Addresses 16-byte aligned, size a multiple of 16.

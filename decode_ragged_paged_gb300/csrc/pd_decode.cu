@@ -183,7 +183,7 @@ __device__ __forceinline__ bool consumer_sync(uint64_t* bar, uint32_t& phase, in
                                               volatile int* abort, int32_t* status) {
   __syncwarp();
   if (lane == 0) mbar_arrive(bar);
-  const bool ok = mbar_wait(bar, phase & 1u, abort, status);
+  const bool ok = warp_mbar_wait(bar, phase & 1u, abort, status);
   ++phase;
   return ok;
 }
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, PD_DECODE_MIN_BLOCKS) decode_kernel(
       for (int s = 0; s < n_st; ++s, ++ctr) {
         if ((s % kNC) != cw) continue;
         const int slot = ctr % NS;
-        if (!mbar_wait(&full[slot], (ctr / NS) & 1u, abort, p.status)) goto consumer_done;
+        if (!warp_mbar_wait(&full[slot], (ctr / NS) & 1u, abort, p.status)) goto consumer_done;
         const uint8_t* buf = ring + (size_t)slot * SB;
         float acc[kTPL * GS];
 #pragma unroll
@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, PD_DECODE_MIN_BLOCKS) decode_kernel(
       for (int s = 0; s < n_st; ++s, ++ctr) {
         if ((s % kNC) != cw) continue;
         const int slot = ctr % NS;
-        if (!mbar_wait(&full[slot], (ctr / NS) & 1u, abort, p.status)) goto consumer_done;
+        if (!warp_mbar_wait(&full[slot], (ctr / NS) & 1u, abort, p.status)) goto consumer_done;
         const uint8_t* buf = ring + (size_t)slot * SB;
         const int valid = min(kTS, n_tok - s * kTS);
 #pragma unroll

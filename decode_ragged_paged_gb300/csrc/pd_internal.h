@@ -59,6 +59,38 @@ int32_t decode_heads_per_item(int32_t group, int32_t head_dim);
 // Plans and runs a decode. Returns a pd_status.
 int launch_decode(DecodeParams& p, int32_t kv_dtype, cudaStream_t stream);
 
+// ----------------------------------------------------------------- prefill
+// Workspace of the tensor-core prefill (offsets 256-byte aligned):
+//   hdr      int32[64]     hdr[0] = work items (q tiles x query heads)
+//   rq_list  int2[max_rq]  (request, q tile) ordered by decreasing KV-tile count
+struct PrefillParams {
+  int32_t batch, hq, hkv, group, page_size, num_pages, total_qo, max_qo_len, max_kv_len, causal, o_dtype;
+  int32_t max_rq;
+  float scale_log2;  // softmax scale times log2(e)
+  const int32_t* qo_indptr;
+  const int32_t* kv_len;
+  const int32_t* page_indptr;
+  const int32_t* page_indices;
+  void* o;
+  float* lse;
+  int32_t* hdr;
+  int2* rq_list;
+  int32_t* status;
+};
+
+struct PrefillLayout {
+  size_t hdr, rq_list, total;
+  int32_t max_rq;
+};
+
+PrefillLayout prefill_layout(int32_t batch, int32_t total_qo, int32_t max_qo_len);
+
+// Checks what the tensor-core prefill supports; returns a pd_status.
+int prefill_supported(int32_t kv_dtype, int32_t head_dim, int32_t page_size);
+
+// Plans and runs a prefill over bf16 q / pools. Returns a pd_status.
+int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const void* v_pool, cudaStream_t stream);
+
 // --------------------------------------------------------------- KV copies
 struct KvCopyParams {
   int32_t batch, hkv, head_dim, page_size, num_layers, num_pages, elem_size;

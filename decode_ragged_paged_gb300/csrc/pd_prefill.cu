@@ -1,0 +1,550 @@
+// pd_prefill.cu -- causal (or full) prefill attention over an HND paged KV
+// cache on the 5th-generation tensor cores (tcgen05, accumulators in TMEM).
+//
+// Perplexity, "Disaggregated prefill and decode" (2025), section "Prefill vs
+// Decode performance": prefill requests bring many tokens (large qo_len) and
+// are compute bound, their attention being GEMM-shaped along the query axis.
+// Query rows of a request are the last qo_len positions of its kv_len cached
+// tokens, so row i may attend keys j <= kv_len - qo_len + i.
+//
+// One persistent CTA per SM walks a list of (request, 128-row q tile, query
+// head) items, heaviest first. Warp roles:
+//   warp 0    TMA producer: Q tile (double buffered), then K and V tiles of 128
+//             tokens (2-slot rings), each tile as one 128-byte-swizzled box per
+//             page and 64-column half; boxes past the request's pages are
+//             fetched out of range and arrive as zeros;
+//   warp 1    allocates 512 TMEM columns and issues tcgen05.mma:
+//             S = Q K^T into one of two S buffers, O += P V into the O buffer;
+//   warps 2-5 one query row per thread: online softmax on S read from TMEM,
+//             P (bf16) written to a swizzled shared tile for the P V product,
+//             O rescaled in TMEM only when the running max grows by more than
+//             2^8, final O / l and log-sum-exp written out.
+// Every wait is bounded; on a timeout the CTA records PD_DEV_TIMEOUT, drains
+// and frees its TMEM.
+#include <math.h>
+
+#include "pd_common.cuh"
+#include "pd_internal.h"
+#include "pd_tc.cuh"
+
+namespace pd {
+
+namespace {
+
+constexpr int kBM = 128;          // query rows per tile
+constexpr int kBN = 128;          // keys per tile
+constexpr int kD = 128;           // head_dim
+constexpr int kThreadsPf = 192;   // 6 warps
+constexpr uint32_t kTileBytes = kBM * kD * 2;  // one bf16 128 x 128 tile
+constexpr uint32_t kHalf = kTileBytes / 2;     // one 64-column half: 128 rows x 128 B
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr float kRescaleThreshold = 8.0f;      // log2 units
+constexpr int kBuckets = 1024;
+
+// shared-memory map (offsets from a 1024-byte aligned base)
+constexpr uint32_t kOffQ = 0;                  // 2 tiles
+constexpr uint32_t kOffP = 2 * kTileBytes;     // 1 tile
+constexpr uint32_t kOffK = 3 * kTileBytes;     // 2 tiles
+constexpr uint32_t kOffV = 5 * kTileBytes;     // 2 tiles
+constexpr uint32_t kOffBar = 7 * kTileBytes;
+constexpr size_t kPrefillSmem = 7 * kTileBytes + 256 + 1024;
+
+struct Bars {
+  uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t s_full[2], s_empty[2], p_full, pv_done, drain;
+  uint32_t tmem_slot;
+  int abort;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+struct PItem {
+  int r, qt, h, g, q0, rows, qo_len, kv, n_kv, pbase, need;
+};
+
+__device__ __forceinline__ int kv_tiles(int qt, int qo_len, int kv, int causal) {
+  if (kv <= 0) return 0;
+  int last_key = kv - 1;
+  if (causal) {
+    const int last_row = min(qt * kBM + kBM - 1, qo_len - 1);
+    last_key = min(last_key, kv - qo_len + last_row);
+  }
+  return last_key < 0 ? 0 : last_key / kBN + 1;
+}
+
+__device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int it) {
+  PItem I;
+  const int rq = it / p.hq;
+  I.h = it - rq * p.hq;
+  const int2 v = p.rq_list[rq];
+  I.r = v.x;
+  I.qt = v.y;
+  I.g = I.h / p.group;
+  const int a = p.qo_indptr[I.r];
+  I.qo_len = p.qo_indptr[I.r + 1] - a;
+  I.q0 = a + I.qt * kBM;
+  I.rows = min(kBM, I.qo_len - I.qt * kBM);
+  I.kv = p.kv_len[I.r];
+  I.n_kv = kv_tiles(I.qt, I.qo_len, I.kv, p.causal);
+  I.pbase = p.page_indptr[I.r];
+  I.need = (I.kv + p.page_size - 1) / p.page_size;
+  return I;
+}
+
+__device__ __forceinline__ bool request_ok(const PrefillParams& p, int r) {
+  const int a = p.qo_indptr[r], b = p.qo_indptr[r + 1];
+  const int n = p.kv_len[r];
+  int code = 0;
+  if (a < 0 || b < a || b > p.total_qo) code = PD_DEV_BAD_INDPTR;
+  else if (n < 0 || n > p.max_kv_len || b - a > p.max_qo_len || (p.causal && b - a > n)) code = PD_DEV_BAD_LENGTH;
+  else {
+    const int pa = p.page_indptr[r], pb = p.page_indptr[r + 1];
+    if (pa < 0 || pb < pa) code = PD_DEV_BAD_INDPTR;
+    else if ((long long)(pb - pa) * p.page_size < n) code = PD_DEV_BAD_PAGE_TABLE;
+  }
+  if (code) report(p.status, code);
+  return code == 0;
+}
+
+// Loads one 128-token K or V tile: per 64-column half, one box per page (or one
+// box of 128 slots when a page holds at least 128 tokens).
+__device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const PItem& I, int j, const CUtensorMap* map,
+                                             uint8_t* dst, uint64_t* bar, int lane) {
+  const int pb = p.page_size < kBN ? p.page_size : kBN;  // slots per box
+  const int nb = kBN / pb;                                // boxes per half
+  const int t0 = j * kBN;
+  int pid = p.num_pages, soff = 0;                        // out of range: zero fill
+  if (lane < nb) {
+    const int pidx = (t0 + lane * pb) / p.page_size;
+    soff = (t0 + lane * pb) % p.page_size;
+    if (pidx < I.need) {
+      pid = __ldg(p.page_indices + I.pbase + pidx);
+      if (pid < 0 || pid >= p.num_pages) {
+        report(p.status, PD_DEV_BAD_PAGE_TABLE);
+        pid = p.num_pages;
+      }
+    }
+  }
+  if (lane == 0) mbar_arrive_expect_tx(bar, kTileBytes);
+  __syncwarp();
+  if (lane < nb) {
+    tma_load_4d(dst + lane * pb * 128, map, 0, soff, I.g, pid, bar);
+    tma_load_4d(dst + kHalf + lane * pb * 128, map, 64, soff, I.g, pid, bar);
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------- plan
+// One CTA: validate, then order the (request, q tile) pairs by decreasing
+// number of KV tiles (counting sort) so that the heaviest items start first.
+__global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams p) {
+  __shared__ int hist[kBuckets];
+  __shared__ int cursor[kBuckets];
+  const int tid = threadIdx.x;
+  for (int b = tid; b < kBuckets; b += blockDim.x) hist[b] = 0;
+  __syncthreads();
+  for (int r = tid; r < p.batch; r += blockDim.x) {
+    if (!request_ok(p, r)) continue;
+    const int qo = p.qo_indptr[r + 1] - p.qo_indptr[r], n = p.kv_len[r];
+    for (int qt = 0; qt * kBM < qo; ++qt) atomicAdd(&hist[min(kv_tiles(qt, qo, n, p.causal), kBuckets - 1)], 1);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int b = kBuckets - 1; b >= 0; --b) {
+      cursor[b] = acc;
+      acc += hist[b];
+    }
+    p.hdr[0] = min(acc, p.max_rq) * p.hq;
+  }
+  __syncthreads();
+  for (int r = tid; r < p.batch; r += blockDim.x) {
+    if (!request_ok(p, r)) continue;
+    const int qo = p.qo_indptr[r + 1] - p.qo_indptr[r], n = p.kv_len[r];
+    for (int qt = 0; qt * kBM < qo; ++qt) {
+      const int pos = atomicAdd(&cursor[min(kv_tiles(qt, qo, n, p.causal), kBuckets - 1)], 1);
+      if (pos < p.max_rq) p.rq_list[pos] = make_int2(r, qt);
+    }
+  }
+}
+
+// ----------------------------------------------------------------- kernel
+__global__ void __launch_bounds__(kThreadsPf, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base + kOffQ;
+  uint8_t* sP = base + kOffP;
+  uint8_t* sK = base + kOffK;
+  uint8_t* sV = base + kOffV;
+  Bars* bars = reinterpret_cast<Bars*>(base + kOffBar);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_empty[i], 4);
+    }
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  const int n_items = p.hdr[0];
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- producer
+    uint32_t it_ctr = 0, kv_ctr = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++it_ctr) {
+      const PItem I = prefill_item(p, it);
+      const int qb = it_ctr & 1;
+      if (!warp_mbar_wait(&bars->q_empty[qb], ((it_ctr >> 1) & 1u) ^ 1u, abort, p.status)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->q_full[qb], kTileBytes);
+        tma_load_3d(sQ + qb * kTileBytes, &tm_q, 0, I.h, I.q0, &bars->q_full[qb]);
+        tma_load_3d(sQ + qb * kTileBytes + kHalf, &tm_q, 64, I.h, I.q0, &bars->q_full[qb]);
+      }
+      __syncwarp();
+      bool ok = true;
+      for (int j = 0; j < I.n_kv && ok; ++j, ++kv_ctr) {
+        const int slot = kv_ctr & 1;
+        const uint32_t par = ((kv_ctr >> 1) & 1u) ^ 1u;
+        ok = warp_mbar_wait(&bars->k_empty[slot], par, abort, p.status);
+        if (!ok) break;
+        load_kv_tile(p, I, j, &tm_k, sK + slot * kTileBytes, &bars->k_full[slot], lane);
+        ok = warp_mbar_wait(&bars->v_empty[slot], par, abort, p.status);
+        if (!ok) break;
+        load_kv_tile(p, I, j, &tm_v, sV + slot * kTileBytes, &bars->v_full[slot], lane);
+      }
+      if (!ok) break;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, 1);
+    const uint32_t sQa = smem_u32(sQ), sPa = smem_u32(sP), sKa = smem_u32(sK), sVa = smem_u32(sV);
+    uint32_t it_ctr = 0, kv_ctr = 0, s_ctr = 0, pv_ctr = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++it_ctr) {
+      const PItem I = prefill_item(p, it);
+      const int qb = it_ctr & 1;
+      ok = warp_mbar_wait(&bars->q_full[qb], (it_ctr >> 1) & 1u, abort, p.status);
+      if (!ok) break;
+      tc_fence_after();
+      int prev_slot = 0;
+      uint32_t prev_par = 0;
+      for (int j = 0; j <= I.n_kv; ++j) {
+        int slot = 0;
+        uint32_t par = 0;
+        if (j < I.n_kv) {
+          slot = kv_ctr & 1;
+          par = (kv_ctr >> 1) & 1u;
+          const int sb = s_ctr & 1;
+          ok = warp_mbar_wait(&bars->k_full[slot], par, abort, p.status) &&
+               warp_mbar_wait(&bars->s_empty[sb], ((s_ctr >> 1) & 1u) ^ 1u, abort, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t qa = sQa + qb * kTileBytes, ka = sKa + slot * kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t off = (kk / 4) * kHalf + (kk % 4) * 32;
+              tc_mma_f16(tmem + (sb ? kColS1 : kColS0), sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024),
+                         idesc_s, kk > 0);
+            }
+            tc_commit(&bars->s_full[sb]);
+            tc_commit(&bars->k_empty[slot]);
+            if (j == I.n_kv - 1) tc_commit(&bars->q_empty[qb]);
+          }
+          __syncwarp();
+        }
+        if (j > 0) {
+          ok = warp_mbar_wait(&bars->p_full, pv_ctr & 1u, abort, p.status) &&
+               warp_mbar_wait(&bars->v_full[prev_slot], prev_par, abort, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t va = sVa + prev_slot * kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk) {
+              tc_mma_f16(tmem + kColO, sw128_desc(sPa + (kk / 4) * kHalf + (kk % 4) * 32, 16, 1024),
+                         sw128_desc(va + kk * 2048, kHalf, 1024), idesc_pv, (j > 1 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(&bars->pv_done);
+            tc_commit(&bars->v_empty[prev_slot]);
+          }
+          __syncwarp();
+          ++pv_ctr;
+        }
+        if (j < I.n_kv) {
+          prev_slot = slot;
+          prev_par = par;
+          ++kv_ctr;
+          ++s_ctr;
+        }
+      }
+      if (ok && I.n_kv == 0 && lane == 0) tc_commit(&bars->q_empty[qb]);
+      __syncwarp();
+    }
+    // all MMAs of this thread complete before TMEM is released
+    if (lane == 0) {
+      tc_commit(&bars->drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&bars->drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------- softmax / epilogue
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+    uint32_t kv_ctr = 0, s_ctr = 0, pv_ctr = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const PItem I = prefill_item(p, it);
+      const int lim = I.kv - I.qo_len + I.qt * kBM + row;  // last key this row may see (causal)
+      // l: sum of the bf16-rounded weights that enter P V (normalises O so its
+      // weights sum to one); l_exact: sum of the unrounded weights (for the lse)
+      float m = -INFINITY, l = 0.f, l_exact = 0.f;
+      for (int j = 0; j < I.n_kv; ++j) {
+        const int sb = s_ctr & 1;
+        ok = warp_mbar_wait(&bars->s_full[sb], (s_ctr >> 1) & 1u, abort, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        const int k0 = j * kBN;
+        int ncol = min(kBN, I.kv - k0);
+        if (p.causal) ncol = min(ncol, lim - k0 + 1);
+        const uint32_t s_addr = t_lane + (sb ? kColS1 : kColS0);
+        // pass 1: row max of the tile
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(s_addr + c * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e < ncol) mt = fmaxf(mt, __uint_as_float(v[e]));
+        }
+        float m_new = m;
+        bool rescale = false;
+        if (mt > -INFINITY) {
+          const float ms = mt * p.scale_log2;
+          if (m == -INFINITY) {
+            m_new = ms;
+          } else if (ms > m + kRescaleThreshold) {
+            m_new = ms;
+            rescale = true;
+          }
+        }
+        // the previous P V product must be complete: O is stable and P is free
+        if (j > 0) {
+          ok = warp_mbar_wait(&bars->pv_done, pv_ctr & 1u, abort, p.status);
+          if (!ok) break;
+          ++pv_ctr;
+          tc_fence_after();
+        }
+        // tcgen05.ld / st are warp-collective: the whole warp rescales its rows of
+        // O when any of them needs it (factor 1 for the others)
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float alpha = rescale ? exp2f(m - m_new) : 1.0f;
+          l *= alpha;
+          l_exact *= alpha;
+#pragma unroll
+          for (int c = 0; c < kD / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(t_lane + kColO + c * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st32(t_lane + kColO + c * 32, v);
+          }
+          tmem_wait_st();
+        }
+        m = m_new;
+        // pass 2: P = exp2(s * scale - m) in bf16, row sum of the rounded values
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(s_addr + c * 32, v);
+          tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int col = c * 32 + e;
+            const float p0 = col < ncol ? exp2f(fmaf(__uint_as_float(v[e]), p.scale_log2, -m)) : 0.f;
+            const float p1 = col + 1 < ncol ? exp2f(fmaf(__uint_as_float(v[e + 1]), p.scale_log2, -m)) : 0.f;
+            w[e / 2] = pack_bf16x2(p0, p1);
+            l += bf16_lo(w[e / 2]) + bf16_hi(w[e / 2]);
+            l_exact += p0 + p1;
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int lc = c * 4 + k;  // 16-byte chunk of the 256-byte P row
+            const uint32_t addr = smem_u32(sP) + (lc / 8) * kHalf + row * 128 + (((lc % 8) ^ (row & 7)) * 16);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * k]), "r"(w[4 * k + 1]),
+                         "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
+                         : "memory");
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_empty[sb]);
+        // keys past kv_len in the last tile: their V rows are zeroed so that
+        // stale values cannot reach O through a zero weight
+        const int valid = I.kv - k0;
+        if (valid < kBN) {
+          const int slot = kv_ctr & 1;
+          ok = warp_mbar_wait(&bars->v_full[slot], (kv_ctr >> 1) & 1u, abort, p.status);
+          if (!ok) break;
+          uint8_t* vt = sV + slot * kTileBytes;
+          const int nchunks = (kBN - valid) * 16;
+          for (int i = threadIdx.x - 64; i < nchunks; i += 128) {
+            const int rr = valid + i / 16, c16 = i % 16;
+            const uint32_t addr = smem_u32(vt) + (c16 / 8) * kHalf + rr * 128 + (c16 % 8) * 16;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full);
+        ++s_ctr;
+        ++kv_ctr;
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l and the log-sum-exp
+      if (I.n_kv > 0) {
+        ok = warp_mbar_wait(&bars->pv_done, pv_ctr & 1u, abort, p.status);
+        if (!ok) break;
+        ++pv_ctr;
+        tc_fence_after();
+      }
+      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+      const bool store = row < I.rows;
+      const int64_t orow = ((int64_t)(I.q0 + row) * p.hq + I.h) * kD;
+#pragma unroll
+      for (int c = 0; c < kD / 32; ++c) {
+        uint32_t v[32];
+        if (I.n_kv > 0) {
+          tmem_ld32(t_lane + kColO + c * 32, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        if (store) {
+          if (p.o_dtype == PD_BF16) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow + c * 32);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint4 u;
+              u.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l);
+              u.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l);
+              u.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l);
+              u.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l);
+              dst[k] = u;
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow + c * 32);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              dst[k] = make_float4(__uint_as_float(v[4 * k]) * inv_l, __uint_as_float(v[4 * k + 1]) * inv_l,
+                                   __uint_as_float(v[4 * k + 2]) * inv_l, __uint_as_float(v[4 * k + 3]) * inv_l);
+          }
+        }
+      }
+      if (store && p.lse != nullptr)
+        p.lse[(int64_t)(I.q0 + row) * p.hq + I.h] =
+            (I.n_kv > 0 && l_exact > 0.f) ? (m + log2f(l_exact)) * kLn2 : -INFINITY;
+      tc_fence_before();
+    }
+  }
+
+  // Normally every copy has been consumed here. After an abort, copies may still
+  // be in flight: give them a bounded 2 ms to land before shared memory is freed.
+  if (*abort && warp == 0 && lane == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 2000000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------- host
+PrefillLayout prefill_layout(int32_t batch, int32_t total_qo, int32_t max_qo_len) {
+  PrefillLayout L{};
+  const int64_t by_len = (int64_t)batch * ((max_qo_len + kBM - 1) / kBM);
+  const int64_t by_rows = (int64_t)(total_qo + kBM - 1) / kBM + batch;
+  L.max_rq = (int32_t)(by_len < by_rows ? by_len : by_rows);
+  if (L.max_rq < 1) L.max_rq = 1;
+  size_t off = 0;
+  L.hdr = off;
+  off = align_up(off + 64 * sizeof(int32_t), 256);
+  L.rq_list = off;
+  off = align_up(off + sizeof(int2) * (size_t)L.max_rq, 256);
+  L.total = off;
+  return L;
+}
+
+int prefill_supported(int32_t kv_dtype, int32_t head_dim, int32_t page_size) {
+  if (kv_dtype != PD_BF16 || head_dim != kD) return PD_ERR_UNSUPPORTED;
+  // page sizes that tile a 128-token block with whole boxes (powers of two >= 8)
+  if (page_size < 8 || (page_size & (page_size - 1)) != 0) return PD_ERR_UNSUPPORTED;
+  return PD_OK;
+}
+
+int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const void* v_pool, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  const int pb = p.page_size < kBN ? p.page_size : kBN;
+  if (!make_rows_map(&tq, q, PD_BF16, p.total_qo, p.hq, kD, 64, kBM, true) ||
+      !make_pool_map(&tk, k_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true) ||
+      !make_pool_map(&tv, v_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true))
+    return PD_ERR_CUDA;
+  static int configured_device = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;
+  if (configured_device != dev) {
+    if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrefillSmem) !=
+        cudaSuccess)
+      return PD_ERR_CUDA;
+    configured_device = dev;
+  }
+  prefill_plan_kernel<<<1, 1024, 0, stream>>>(p);
+  int64_t grid = device_sm_count();
+  const int64_t max_items = (int64_t)p.max_rq * p.hq;
+  if (grid > max_items) grid = max_items;
+  if (grid < 1) grid = 1;
+  profile_begin(stream);
+  prefill_kernel<<<(unsigned)grid, kThreadsPf, kPrefillSmem, stream>>>(tq, tk, tv, p);
+  profile_end(stream);
+  return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
+}
+
+}  // namespace pd

@@ -1,0 +1,124 @@
+"""GPU parity of pd_attn_prefill (tcgen05 tensor-core path) against the fp64
+oracle on the same seeded bf16 inputs.
+
+Tolerance (benchmark spec): max |o - oracle| <= 1e-2 with fp32
+accumulation, |lse - oracle| <= 1e-3. With a bf16 output the stored value is
+additionally rounded to bf16, which alone moves it by up to half a bf16 ulp of
+|o|; the bf16-output checks allow that rounding on top of 1e-2."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import decode_ragged_paged_gb300 as pd
+    from gpu_util import DevCase, LSE_TOL, host_f64
+
+
+def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
+    return 2.0 ** (e - 8)
+
+
+def run_prefill(case, o_dtype=torch.float32, status=None):
+    d = DevCase(case)
+    o, lse = pd.pd_attn_prefill(d.q, d.k_pool, d.v_pool, d.kv_len, d.page_indptr, d.page_indices, d.qo_indptr,
+                                causal=case.causal, sm_scale=case.sm_scale, max_qo_len=d.max_qo_len,
+                                max_kv_len=d.max_kv_len, o_dtype=o_dtype, dev_status=status)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def check(case, o_dtype=torch.float32, ref=None):
+    o, lse = run_prefill(case, o_dtype)
+    o_ref, lse_ref = ref if ref is not None else oracle.attention_case(case)
+    got = host_f64(o)
+    assert np.isfinite(got).all(), "non-finite output"
+    err = np.abs(got - o_ref)
+    bound = 1e-2 + (half_ulp_bf16(o_ref) if o_dtype == torch.bfloat16 else 0.0)
+    assert np.all(err <= bound), f"max |o - oracle| = {err.max()} (max allowed {bound.max()})"
+    lg = lse.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lg), fin)
+    lerr = float(np.abs(lg[fin] - lse_ref[fin]).max()) if fin.any() else 0.0
+    assert lerr <= LSE_TOL, f"max |lse - oracle| = {lerr}"
+    return float(err.max()), lerr
+
+
+def test_prefill_single_tile():
+    check(wl.make_attn_case(301, [100], [100], 2, 2, 128, 16, wl.BF16, causal=True, num_pages=8))
+
+
+def test_causal_prefill_workload_full():
+    # 8 requests x 512 tokens, 40 = 40 heads, D 128, page 16, bf16; K/V appended first
+    case = wl.causal_prefill()
+    d = DevCase(case)
+    pd.pd_kv_append(d.k_new, d.v_new, d.k_pool, d.v_pool, d.qo_indptr, d.kv_len, d.page_indptr, d.page_indices,
+                    max_kv_len=512)
+    full = wl.make_attn_case(3, [512] * 8, [512] * 8, 40, 40, 128, 16, wl.BF16, causal=True)
+    assert np.array_equal(d.k_pool.view(torch.int16).cpu().numpy().view(np.uint16), full.k_pool)
+    ref = oracle.attention_case(full)
+    o, lse = pd.pd_attn_prefill(d.q, d.k_pool, d.v_pool, d.kv_len, d.page_indptr, d.page_indices, d.qo_indptr,
+                                max_qo_len=512, max_kv_len=512, o_dtype=torch.float32)
+    torch.cuda.synchronize()
+    err = float(np.abs(host_f64(o) - ref[0]).max())
+    lerr = float(np.abs(lse.cpu().numpy() - ref[1]).max())
+    assert err <= 1e-2 and lerr <= LSE_TOL, (err, lerr)
+    # bf16 output of the same call
+    check(full, torch.bfloat16, ref=ref)
+
+
+@pytest.mark.parametrize("qo,kv,hq,hkv,p,causal", [
+    ([300, 1, 129], [300, 700, 129], 4, 2, 16, True),        # ragged tiles, one decode-like row
+    ([64, 200], [1000, 520], 4, 4, 64, True),               # chunked prefill: qo < kv (bottom-right)
+    ([128, 256], [128, 256], 8, 1, 8, True),                # GQA 8:1, page 8
+    ([90, 40], [333, 41], 2, 2, 128, False),                # no mask, page 128
+    ([257], [2000], 2, 1, 256, True),                       # page 256
+])
+def test_prefill_shapes(qo, kv, hq, hkv, p, causal):
+    case = wl.make_attn_case(302 + sum(qo), qo, kv, hq, hkv, 128, p, wl.BF16, causal=causal)
+    check(case)
+
+
+def test_prefill_empty_kv_non_causal():
+    case = wl.make_attn_case(303, [5, 7], [0, 9], 2, 2, 128, 16, wl.BF16, causal=False, num_pages=3)
+    o, lse = run_prefill(case)
+    assert torch.all(o[:5] == 0) and torch.all(torch.isneginf(lse[:5]))
+    check(case)
+
+
+def test_prefill_growing_scores_rescale_path():
+    # scores rise along the key axis so the running max jumps by more than 2^8
+    # in log2 units between tiles, forcing the O rescale in tensor memory
+    case = wl.make_attn_case(304, [512], [512], 2, 2, 128, 16, wl.BF16, causal=True)
+    n = 512
+    t = np.arange(n)
+    pages = case.table.page_indices
+    q = wl.bf16_to_f32(case.q)
+    q[:, :, 0] = 4.0
+    case.q = wl.bf16_from_f32(q)
+    k = wl.bf16_to_f32(case.k_pool)
+    k[pages[t // 16], :, t % 16, 0] = (t / 4.0)[:, None]           # q.k grows by 1 per key
+    case.k_pool = wl.bf16_from_f32(k)
+    check(case)
+
+
+def test_prefill_bad_length_is_reported():
+    case = wl.make_attn_case(305, [40, 30], [40, 30], 2, 2, 128, 16, wl.BF16, causal=True)
+    d = DevCase(case)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pd.pd_attn_prefill(d.q, d.k_pool, d.v_pool, d.kv_len, d.page_indptr, d.page_indices, d.qo_indptr,
+                       max_qo_len=32, max_kv_len=40, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 2
+
+
+def test_prefill_deterministic():
+    case = wl.make_attn_case(306, [200, 333], [200, 400], 4, 2, 128, 16, wl.BF16, causal=True)
+    a, la = run_prefill(case, torch.bfloat16)
+    b, lb = run_prefill(case, torch.bfloat16)
+    assert torch.equal(a, b) and torch.equal(la, lb)
