@@ -34,25 +34,27 @@ namespace {
 constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per tile
 constexpr int kD = 128;           // head_dim
-constexpr int kThreadsPf = 192;   // 6 warps
+constexpr int kThreadsPf = 224;   // 7 warps: Q/K loads, MMA, 4 softmax, V loads
+constexpr int kWarpV = 6;         // the warp that loads V tiles
 constexpr uint32_t kTileBytes = kBM * kD * 2;  // one bf16 128 x 128 tile
 constexpr uint32_t kHalf = kTileBytes / 2;     // one 64-column half: 128 rows x 128 B
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr int kSB = 3;                         // S / P buffers in TMEM (128 columns each)
+constexpr uint32_t kColO = kSB * 128;          // O accumulator after them
+__device__ __forceinline__ uint32_t col_s(int b) { return (uint32_t)b * 128; }
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 constexpr int kBuckets = 1024;
 
 // shared-memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t kOffQ = 0;                  // 2 tiles
-constexpr uint32_t kOffP = 2 * kTileBytes;     // 1 tile
-constexpr uint32_t kOffK = 3 * kTileBytes;     // 2 tiles
-constexpr uint32_t kOffV = 5 * kTileBytes;     // 2 tiles
-constexpr uint32_t kOffBar = 7 * kTileBytes;
-constexpr size_t kPrefillSmem = 7 * kTileBytes + 256 + 1024;
+constexpr uint32_t kOffK = 2 * kTileBytes;     // 2 tiles
+constexpr uint32_t kOffV = 4 * kTileBytes;     // 2 tiles
+constexpr uint32_t kOffBar = 6 * kTileBytes;
+constexpr size_t kPrefillSmem = 6 * kTileBytes + 256 + 1024;
 
 struct Bars {
   uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[2], s_empty[2], p_full, pv_done, drain;
+  uint64_t s_full[kSB], s_empty[kSB], p_full[kSB], pv_done[kSB], drain;
   uint32_t tmem_slot;
   int abort;
 };
@@ -176,7 +178,6 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base + kOffQ;
-  uint8_t* sP = base + kOffP;
   uint8_t* sK = base + kOffK;
   uint8_t* sV = base + kOffV;
   Bars* bars = reinterpret_cast<Bars*>(base + kOffBar);
@@ -191,11 +192,13 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       mbar_init(&bars->k_empty[i], 1);
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_empty[i], 4);
     }
-    mbar_init(&bars->p_full, 4);
-    mbar_init(&bars->pv_done, 1);
+    for (int i = 0; i < kSB; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_empty[i], 1);
+      mbar_init(&bars->p_full[i], 4);
+      mbar_init(&bars->pv_done[i], 1);
+    }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_barrier_init();
@@ -215,37 +218,47 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
   const uint32_t tmem = bars->tmem_slot;
   const int n_items = p.hdr[0];
 
-  if (warp == 0) {
-    // -------------------------------------------------------------- producer
+  if (warp == 0 || warp == kWarpV) {
+    // ------------------------------------------------------------- producers
+    // Warp 0 loads the Q tile of each item and its K tiles, warp kWarpV its V
+    // tiles: a warp keeps only a few TMA copies in flight, so two issuing warps
+    // double the rate at which a tile's page boxes are requested.
+    const bool is_v = warp == kWarpV;
     uint32_t it_ctr = 0, kv_ctr = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++it_ctr) {
       const PItem I = prefill_item(p, it);
-      const int qb = it_ctr & 1;
-      if (!warp_mbar_wait(&bars->q_empty[qb], ((it_ctr >> 1) & 1u) ^ 1u, abort, p.status)) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->q_full[qb], kTileBytes);
-        tma_load_3d(sQ + qb * kTileBytes, &tm_q, 0, I.h, I.q0, &bars->q_full[qb]);
-        tma_load_3d(sQ + qb * kTileBytes + kHalf, &tm_q, 64, I.h, I.q0, &bars->q_full[qb]);
+      if (!is_v) {
+        const int qb = it_ctr & 1;
+        if (!warp_mbar_wait(&bars->q_empty[qb], ((it_ctr >> 1) & 1u) ^ 1u, abort, p.status)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->q_full[qb], kTileBytes);
+          tma_load_3d(sQ + qb * kTileBytes, &tm_q, 0, I.h, I.q0, &bars->q_full[qb]);
+          tma_load_3d(sQ + qb * kTileBytes + kHalf, &tm_q, 64, I.h, I.q0, &bars->q_full[qb]);
+        }
+        __syncwarp();
       }
-      __syncwarp();
       bool ok = true;
       for (int j = 0; j < I.n_kv && ok; ++j, ++kv_ctr) {
         const int slot = kv_ctr & 1;
         const uint32_t par = ((kv_ctr >> 1) & 1u) ^ 1u;
-        ok = warp_mbar_wait(&bars->k_empty[slot], par, abort, p.status);
-        if (!ok) break;
-        load_kv_tile(p, I, j, &tm_k, sK + slot * kTileBytes, &bars->k_full[slot], lane);
-        ok = warp_mbar_wait(&bars->v_empty[slot], par, abort, p.status);
-        if (!ok) break;
-        load_kv_tile(p, I, j, &tm_v, sV + slot * kTileBytes, &bars->v_full[slot], lane);
+        if (!is_v) {
+          ok = warp_mbar_wait(&bars->k_empty[slot], par, abort, p.status);
+          if (ok) load_kv_tile(p, I, j, &tm_k, sK + slot * kTileBytes, &bars->k_full[slot], lane);
+        } else {
+          ok = warp_mbar_wait(&bars->v_empty[slot], par, abort, p.status);
+          if (ok) load_kv_tile(p, I, j, &tm_v, sV + slot * kTileBytes, &bars->v_full[slot], lane);
+        }
       }
       if (!ok) break;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
+    // S_j = Q K_j^T into TMEM buffer j % kSB; the softmax warps overwrite that
+    // buffer with P_j (bf16), which O += P_j V_j reads as its A operand; the
+    // buffer is free again once that product has completed.
     constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, 1);
-    const uint32_t sQa = smem_u32(sQ), sPa = smem_u32(sP), sKa = smem_u32(sK), sVa = smem_u32(sV);
+    const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
     uint32_t it_ctr = 0, kv_ctr = 0, s_ctr = 0, pv_ctr = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++it_ctr) {
@@ -254,17 +267,17 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       ok = warp_mbar_wait(&bars->q_full[qb], (it_ctr >> 1) & 1u, abort, p.status);
       if (!ok) break;
       tc_fence_after();
-      int prev_slot = 0;
+      int prev_slot = 0, prev_sb = 0;
       uint32_t prev_par = 0;
       for (int j = 0; j <= I.n_kv; ++j) {
-        int slot = 0;
+        int slot = 0, sb = 0;
         uint32_t par = 0;
         if (j < I.n_kv) {
           slot = kv_ctr & 1;
           par = (kv_ctr >> 1) & 1u;
-          const int sb = s_ctr & 1;
+          sb = s_ctr % kSB;
           ok = warp_mbar_wait(&bars->k_full[slot], par, abort, p.status) &&
-               warp_mbar_wait(&bars->s_empty[sb], ((s_ctr >> 1) & 1u) ^ 1u, abort, p.status);
+               warp_mbar_wait(&bars->s_empty[sb], ((s_ctr / kSB) & 1u) ^ 1u, abort, p.status);
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
@@ -272,8 +285,8 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk) {
               const uint32_t off = (kk / 4) * kHalf + (kk % 4) * 32;
-              tc_mma_f16(tmem + (sb ? kColS1 : kColS0), sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024),
-                         idesc_s, kk > 0);
+              tc_mma_f16(tmem + col_s(sb), sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024), idesc_s,
+                         kk > 0);
             }
             tc_commit(&bars->s_full[sb]);
             tc_commit(&bars->k_empty[slot]);
@@ -282,19 +295,36 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
           __syncwarp();
         }
         if (j > 0) {
-          ok = warp_mbar_wait(&bars->p_full, pv_ctr & 1u, abort, p.status) &&
+          const uint32_t pt = s_ctr - 1;  // running index of tile j - 1
+          ok = warp_mbar_wait(&bars->p_full[prev_sb], (pt / kSB) & 1u, abort, p.status) &&
                warp_mbar_wait(&bars->v_full[prev_slot], prev_par, abort, p.status);
           if (!ok) break;
+          // keys past kv_len in the request's last tile: zero their V rows so that
+          // stale values cannot reach O through a zero weight
+          const int valid = I.kv - (j - 1) * kBN;
+          if (valid < kBN) {
+            const uint32_t vt = smem_u32(sV + prev_slot * kTileBytes);
+            for (int i = lane; i < (kBN - valid) * 16; i += 32) {
+              const int rr = valid + i / 16, c16 = i % 16;
+              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vt + (c16 / 8) * kHalf + rr * 128 +
+                                                                          (c16 % 8) * 16),
+                           "r"(0)
+                           : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
           tc_fence_after();
           if (lane == 0) {
             const uint32_t va = sVa + prev_slot * kTileBytes;
+            const uint32_t pa = tmem + col_s(prev_sb);  // P: 64 columns of bf16 pairs
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-              tc_mma_f16(tmem + kColO, sw128_desc(sPa + (kk / 4) * kHalf + (kk % 4) * 32, 16, 1024),
-                         sw128_desc(va + kk * 2048, kHalf, 1024), idesc_pv, (j > 1 || kk > 0) ? 1u : 0u);
-            }
-            tc_commit(&bars->pv_done);
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              tc_mma_f16_tmem_a(tmem + kColO, pa + 8 * kk, sw128_desc(va + kk * 2048, kHalf, 1024), idesc_pv,
+                                (j > 1 || kk > 0) ? 1u : 0u);
+            tc_commit(&bars->pv_done[prev_sb]);
             tc_commit(&bars->v_empty[prev_slot]);
+            tc_commit(&bars->s_empty[prev_sb]);
           }
           __syncwarp();
           ++pv_ctr;
@@ -302,6 +332,7 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         if (j < I.n_kv) {
           prev_slot = slot;
           prev_par = par;
+          prev_sb = sb;
           ++kv_ctr;
           ++s_ctr;
         }
@@ -317,12 +348,12 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2 && warp < 6) {
     // --------------------------------------------------- softmax / epilogue
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-    uint32_t kv_ctr = 0, s_ctr = 0, pv_ctr = 0;
+    uint32_t s_ctr = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const PItem I = prefill_item(p, it);
@@ -331,25 +362,36 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       // weights sum to one); l_exact: sum of the unrounded weights (for the lse)
       float m = -INFINITY, l = 0.f, l_exact = 0.f;
       for (int j = 0; j < I.n_kv; ++j) {
-        const int sb = s_ctr & 1;
-        ok = warp_mbar_wait(&bars->s_full[sb], (s_ctr >> 1) & 1u, abort, p.status);
+        const int sb = s_ctr % kSB;
+        ok = warp_mbar_wait(&bars->s_full[sb], (s_ctr / kSB) & 1u, abort, p.status);
         if (!ok) break;
         tc_fence_after();
         const int k0 = j * kBN;
         int ncol = min(kBN, I.kv - k0);
         if (p.causal) ncol = min(ncol, lim - k0 + 1);
-        const uint32_t s_addr = t_lane + (sb ? kColS1 : kColS0);
-        // pass 1: row max of the tile
-        float mt = -INFINITY;
+        const uint32_t s_addr = t_lane + col_s(sb);
+        // the whole S row in registers: four loads, one wait
+        uint32_t v[kBN];
+        tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
+        tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
+        tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+        tmem_wait_ld();
+        // row max of the tile (four independent chains); columns past ncol are
+        // masked only in tiles where some row of the warp has any
+        const bool full_tile = __all_sync(0xffffffffu, ncol >= kBN);
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (full_tile) {
 #pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(s_addr + c * 32, v);
-          tmem_wait_ld();
+          for (int e = 0; e < kBN; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(v[e]));
+        } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e < ncol) mt = fmaxf(mt, __uint_as_float(v[e]));
+          for (int e = 0; e < kBN; ++e) {
+            const float x = __uint_as_float(v[e]);
+            mx[e & 3] = fmaxf(mx[e & 3], e < ncol ? x : -INFINITY);
+          }
         }
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         float m_new = m;
         bool rescale = false;
         if (mt > -INFINITY) {
@@ -361,125 +403,105 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
             rescale = true;
           }
         }
-        // the previous P V product must be complete: O is stable and P is free
-        if (j > 0) {
-          ok = warp_mbar_wait(&bars->pv_done, pv_ctr & 1u, abort, p.status);
-          if (!ok) break;
-          ++pv_ctr;
-          tc_fence_after();
-        }
         // tcgen05.ld / st are warp-collective: the whole warp rescales its rows of
-        // O when any of them needs it (factor 1 for the others)
+        // O when any of them needs it (factor 1 for the others), after the
+        // previous P V product has completed. That product's barrier (buffer of
+        // tile s_ctr - 1) cannot move past this phase before this tile's P is
+        // published, so waiting only when needed keeps the phase count exact.
         if (__any_sync(0xffffffffu, rescale)) {
+          const uint32_t prev = s_ctr - 1;
+          ok = warp_mbar_wait(&bars->pv_done[prev % kSB], (prev / kSB) & 1u, abort, p.status);
+          if (!ok) break;
+          tc_fence_after();
           const float alpha = rescale ? exp2f(m - m_new) : 1.0f;
           l *= alpha;
           l_exact *= alpha;
 #pragma unroll
           for (int c = 0; c < kD / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(t_lane + kColO + c * 32, v);
+            uint32_t o[32];
+            tmem_ld32(t_lane + kColO + c * 32, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tmem_st32(t_lane + kColO + c * 32, v);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(t_lane + kColO + c * 32, o);
           }
           tmem_wait_st();
         }
         m = m_new;
-        // pass 2: P = exp2(s * scale - m) in bf16, row sum of the rounded values
+        // P = 2^(s * scale - m) as bf16 pairs, written over the S columns; masked
+        // columns get the argument -inf (weight 0). Sums in packed pairs.
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m, -m);
+        float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        float2 le2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        uint32_t w[kBN / 2];
 #pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(s_addr + c * 32, v);
-          tmem_wait_ld();
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int col = c * 32 + e;
-            const float p0 = col < ncol ? exp2f(fmaf(__uint_as_float(v[e]), p.scale_log2, -m)) : 0.f;
-            const float p1 = col + 1 < ncol ? exp2f(fmaf(__uint_as_float(v[e + 1]), p.scale_log2, -m)) : 0.f;
-            w[e / 2] = pack_bf16x2(p0, p1);
-            l += bf16_lo(w[e / 2]) + bf16_hi(w[e / 2]);
-            l_exact += p0 + p1;
+        for (int e = 0; e < kBN; e += 2) {
+          float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nm2);
+          if (!full_tile) {
+            x.x = e < ncol ? x.x : -INFINITY;
+            x.y = e + 1 < ncol ? x.y : -INFINITY;
           }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int lc = c * 4 + k;  // 16-byte chunk of the 256-byte P row
-            const uint32_t addr = smem_u32(sP) + (lc / 8) * kHalf + row * 128 + (((lc % 8) ^ (row & 7)) * 16);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * k]), "r"(w[4 * k + 1]),
-                         "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
-                         : "memory");
-          }
+          const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          const uint32_t pk = pack_bf16x2(pe.x, pe.y);
+          w[e / 2] = pk;
+          ls2[(e / 2) & 1] = fadd2(ls2[(e / 2) & 1], make_float2(bf16_lo(pk), bf16_hi(pk)));
+          le2[(e / 2) & 1] = fadd2(le2[(e / 2) & 1], pe);
         }
+        l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
+        l_exact += (le2[0].x + le2[0].y) + (le2[1].x + le2[1].y);
+        tmem_st32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(w + 0));
+        tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(w + 32));
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->s_empty[sb]);
-        // keys past kv_len in the last tile: their V rows are zeroed so that
-        // stale values cannot reach O through a zero weight
-        const int valid = I.kv - k0;
-        if (valid < kBN) {
-          const int slot = kv_ctr & 1;
-          ok = warp_mbar_wait(&bars->v_full[slot], (kv_ctr >> 1) & 1u, abort, p.status);
-          if (!ok) break;
-          uint8_t* vt = sV + slot * kTileBytes;
-          const int nchunks = (kBN - valid) * 16;
-          for (int i = threadIdx.x - 64; i < nchunks; i += 128) {
-            const int rr = valid + i / 16, c16 = i % 16;
-            const uint32_t addr = smem_u32(vt) + (c16 / 8) * kHalf + rr * 128 + (c16 % 8) * 16;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->p_full);
+        if (lane == 0) mbar_arrive(&bars->p_full[sb]);
         ++s_ctr;
-        ++kv_ctr;
       }
       if (!ok) break;
-      // ---- epilogue: O / l and the log-sum-exp
+      // ---- epilogue: O / l and the log-sum-exp, once the last P V is done
       if (I.n_kv > 0) {
-        ok = warp_mbar_wait(&bars->pv_done, pv_ctr & 1u, abort, p.status);
+        const uint32_t last = s_ctr - 1;
+        ok = warp_mbar_wait(&bars->pv_done[last % kSB], (last / kSB) & 1u, abort, p.status);
         if (!ok) break;
-        ++pv_ctr;
         tc_fence_after();
       }
       const float inv_l = l > 0.f ? 1.0f / l : 0.f;
       const bool store = row < I.rows;
       const int64_t orow = ((int64_t)(I.q0 + row) * p.hq + I.h) * kD;
+      uint32_t v[kD];
+      if (I.n_kv > 0) {
+        tmem_ld32(t_lane + kColO + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
+        tmem_ld32(t_lane + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld32(t_lane + kColO + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
+        tmem_ld32(t_lane + kColO + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+        tmem_wait_ld();
+      } else {
 #pragma unroll
-      for (int c = 0; c < kD / 32; ++c) {
-        uint32_t v[32];
-        if (I.n_kv > 0) {
-          tmem_ld32(t_lane + kColO + c * 32, v);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = 0u;
-        }
-        if (store) {
-          if (p.o_dtype == PD_BF16) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow + c * 32);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint4 u;
-              u.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l);
-              u.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l);
-              u.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l);
-              u.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l);
-              dst[k] = u;
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow + c * 32);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              dst[k] = make_float4(__uint_as_float(v[4 * k]) * inv_l, __uint_as_float(v[4 * k + 1]) * inv_l,
-                                   __uint_as_float(v[4 * k + 2]) * inv_l, __uint_as_float(v[4 * k + 3]) * inv_l);
-          }
-        }
+        for (int e = 0; e < kD; ++e) v[e] = 0u;
       }
-      if (store && p.lse != nullptr)
-        p.lse[(int64_t)(I.q0 + row) * p.hq + I.h] =
-            (I.n_kv > 0 && l_exact > 0.f) ? (m + log2f(l_exact)) * kLn2 : -INFINITY;
+      if (store) {
+        if (p.o_dtype == PD_BF16) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow);
+#pragma unroll
+          for (int k = 0; k < kD / 8; ++k) {
+            uint4 u;
+            u.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l);
+            u.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l);
+            u.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l);
+            u.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l);
+            dst[k] = u;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow);
+#pragma unroll
+          for (int k = 0; k < kD / 4; ++k)
+            dst[k] = make_float4(__uint_as_float(v[4 * k]) * inv_l, __uint_as_float(v[4 * k + 1]) * inv_l,
+                                 __uint_as_float(v[4 * k + 2]) * inv_l, __uint_as_float(v[4 * k + 3]) * inv_l);
+        }
+        if (p.lse != nullptr)
+          p.lse[(int64_t)(I.q0 + row) * p.hq + I.h] =
+              (I.n_kv > 0 && l_exact > 0.f) ? (m + log2f(l_exact)) * kLn2 : -INFINITY;
+      }
       tc_fence_before();
     }
   }
