@@ -22,6 +22,7 @@
 // Every wait is bounded; on a timeout the CTA records PD_DEV_TIMEOUT, drains
 // and frees its TMEM.
 #include <math.h>
+#include <string.h>
 
 #include "pd_common.cuh"
 #include "pd_internal.h"
@@ -49,12 +50,13 @@ constexpr int kBuckets = 1024;
 constexpr uint32_t kOffQ = 0;                  // 2 tiles
 constexpr uint32_t kOffK = 2 * kTileBytes;     // 2 tiles
 constexpr uint32_t kOffV = 4 * kTileBytes;     // 2 tiles
-constexpr uint32_t kOffBar = 6 * kTileBytes;
-constexpr size_t kPrefillSmem = 6 * kTileBytes + 256 + 1024;
+constexpr uint32_t kOffO = 6 * kTileBytes;     // 1 tile: bf16 O staged for the TMA store
+constexpr uint32_t kOffBar = 7 * kTileBytes;
+constexpr size_t kPrefillSmem = 7 * kTileBytes + 256 + 1024;
 
 struct Bars {
   uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[kSB], s_empty[kSB], p_full[kSB], pv_done[kSB], drain;
+  uint64_t s_full[kSB], s_empty[kSB], p_full[kSB], pv_done[kSB], drain, o_sync;
   uint32_t tmem_slot;
   int abort;
 };
@@ -174,12 +176,14 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
 // ----------------------------------------------------------------- kernel
 __global__ void __launch_bounds__(kThreadsPf, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base + kOffQ;
   uint8_t* sK = base + kOffK;
   uint8_t* sV = base + kOffV;
+  uint8_t* sO = base + kOffO;
   Bars* bars = reinterpret_cast<Bars*>(base + kOffBar);
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -200,6 +204,7 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       mbar_init(&bars->pv_done[i], 1);
     }
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->o_sync, 4);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -353,7 +358,8 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-    uint32_t s_ctr = 0;
+    uint32_t s_ctr = 0, o_phase = 0;
+    const bool o_issuer = (warp == 2 && lane == 0);
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const PItem I = prefill_item(p, it);
@@ -479,7 +485,39 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
 #pragma unroll
         for (int e = 0; e < kD; ++e) v[e] = 0u;
       }
-      if (store) {
+      if (p.o_dtype == PD_BF16 && I.rows == kBM) {
+        // full tile: stage bf16 O (128-byte swizzled like Q) and write it with
+        // two TMA stores; the staging buffer is reused once the previous
+        // stores have read it
+        if (o_issuer) bulk_wait_read_all();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->o_sync);
+        ok = warp_mbar_wait(&bars->o_sync, o_phase & 1u, abort, p.status);
+        ++o_phase;
+        if (!ok) break;
+        const uint32_t so = smem_u32(sO);
+#pragma unroll
+        for (int k = 0; k < kD / 8; ++k) {
+          const uint32_t a0 = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l);
+          const uint32_t a1 = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l);
+          const uint32_t a2 = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l);
+          const uint32_t a3 = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l);
+          const uint32_t addr = so + (k / 8) * kHalf + row * 128 + (((k % 8) ^ (row & 7)) * 16);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->o_sync);
+        ok = warp_mbar_wait(&bars->o_sync, o_phase & 1u, abort, p.status);
+        ++o_phase;
+        if (!ok) break;
+        if (o_issuer) {
+          tma_store_3d(&tm_o, 0, I.h, I.q0, sO);
+          tma_store_3d(&tm_o, 64, I.h, I.q0, sO + kHalf);
+          bulk_commit_group();
+        }
+      } else if (store) {
         if (p.o_dtype == PD_BF16) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow);
 #pragma unroll
@@ -498,12 +536,13 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
             dst[k] = make_float4(__uint_as_float(v[4 * k]) * inv_l, __uint_as_float(v[4 * k + 1]) * inv_l,
                                  __uint_as_float(v[4 * k + 2]) * inv_l, __uint_as_float(v[4 * k + 3]) * inv_l);
         }
-        if (p.lse != nullptr)
-          p.lse[(int64_t)(I.q0 + row) * p.hq + I.h] =
-              (I.n_kv > 0 && l_exact > 0.f) ? (m + log2f(l_exact)) * kLn2 : -INFINITY;
       }
+      if (store && p.lse != nullptr)
+        p.lse[(int64_t)(I.q0 + row) * p.hq + I.h] =
+            (I.n_kv > 0 && l_exact > 0.f) ? (m + log2f(l_exact)) * kLn2 : -INFINITY;
       tc_fence_before();
     }
+    if (o_issuer) bulk_wait_all();
   }
 
   // Normally every copy has been consumed here. After an abort, copies may still
@@ -543,8 +582,10 @@ int prefill_supported(int32_t kv_dtype, int32_t head_dim, int32_t page_size) {
 }
 
 int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const void* v_pool, cudaStream_t stream) {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const int pb = p.page_size < kBN ? p.page_size : kBN;
+  memset(&to, 0, sizeof(to));
+  if (p.o_dtype == PD_BF16 && !make_rows_map(&to, p.o, PD_BF16, p.total_qo, p.hq, kD, 64, kBM, true)) return PD_ERR_CUDA;
   if (!make_rows_map(&tq, q, PD_BF16, p.total_qo, p.hq, kD, 64, kBM, true) ||
       !make_pool_map(&tk, k_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true) ||
       !make_pool_map(&tv, v_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true))
@@ -564,7 +605,7 @@ int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const vo
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
   profile_begin(stream);
-  prefill_kernel<<<(unsigned)grid, kThreadsPf, kPrefillSmem, stream>>>(tq, tk, tv, p);
+  prefill_kernel<<<(unsigned)grid, kThreadsPf, kPrefillSmem, stream>>>(tq, tk, tv, to, p);
   profile_end(stream);
   return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
 }
