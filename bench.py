@@ -336,14 +336,34 @@ def measure_rows(args, dev, peaks) -> dict:
 
     w = torch_gen.mixed_1p_nd(device=dev)
     kvb = int(w["kv_len_host"].sum()) * 40 * 128 * 2 * 2 + 2 * w["q"].numel() * 2
+    pre = int(w["qo_len_host"][0])
+    dec_kvb = int(w["kv_len_host"][1:].sum()) * 40 * 128 * 2 * 2
+    mflops = 2 * 128 * pre * (pre + 1) * 40 + 4 * 128 * int(w["kv_len_host"][1:].sum()) * 40
     try:
         o = torch.empty_like(w["q"])
         ms, kms = timed(lambda: pd.pd_attn_mixed(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
                                                  w["page_indices"], w["qo_indptr"], max_qo_len=1024,
                                                  max_kv_len=1024, o=o), reps, warm, flush)
+        o_p, o_d = o[:pre], o[pre:]
+
+        def separate():
+            pd.pd_attn_prefill(w["q"][:pre], w["k_pool"], w["v_pool"], w["kv_len"][:1], w["page_indptr"][:2],
+                               w["page_indices"], w["qo_indptr"][:2], max_qo_len=pre, max_kv_len=pre, o=o_p)
+            pd.pd_attn_decode(w["q"][pre:], w["k_pool"], w["v_pool"], w["kv_len"][1:], w["page_indptr"][1:],
+                              w["page_indices"], max_kv_len=576, o=o_d)
+
+        sep_ms, _ = timed(separate, reps, warm, flush, prof=False)
+        dec_ms, dec_kms = timed(lambda: pd.pd_attn_decode(w["q"][pre:], w["k_pool"], w["v_pool"], w["kv_len"][1:],
+                                                          w["page_indptr"][1:], w["page_indices"], max_kv_len=576,
+                                                          o=o_d), reps, warm, flush)
         rows["mixed"] = {"workload": "1 prefill (1024) + 63 decodes (kv U[512,576]), 40 heads, D 128, bf16",
-                         "ms": round(ms, 5), "GBs": round(kvb / kms / 1e6, 1),
-                         "frac_hbm": round(kvb / kms / 1e6 / hbm, 4), "bound": "hbm", "bytes": kvb}
+                         "fused_ms": round(ms, 5), "fused_kernel_ms": round(kms, 5),
+                         "GBs": round(kvb / kms / 1e6, 1), "frac_hbm": round(kvb / kms / 1e6 / hbm, 4),
+                         "TFLOPs": round(mflops / kms / 1e9, 1), "bound": "hbm", "bytes": kvb, "flops": mflops,
+                         "separate_ms": round(sep_ms, 5), "decode_only_ms": round(dec_ms, 5),
+                         "decode_only_GBs": round(dec_kvb / dec_kms / 1e6, 1),
+                         "interference_fused_over_decode_only": round(ms / dec_ms, 3),
+                         "interference_separate_over_decode_only": round(sep_ms / dec_ms, 3)}
     except pd.PdError as e:
         rows["mixed"] = {"status": str(e)}
     del w

@@ -107,7 +107,8 @@ const char* pd_device_status_string(int32_t code) {
 size_t pd_attn_workspace_size(const pd_attn_desc* desc, const pd_batch* batch, int32_t kind) {
   if (check_attn(desc, batch, false) != PD_OK) return 0;
   if (kind == PD_KIND_DECODE) return decode_layout_for(desc, batch).total;
-  if (kind == PD_KIND_PREFILL) return prefill_layout(batch->batch_size, batch->total_qo, batch->max_qo_len).total;
+  if (kind == PD_KIND_PREFILL || kind == PD_KIND_MIXED)
+    return prefill_layout(batch->batch_size, batch->total_qo, batch->max_qo_len).total;
   return 0;
 }
 
@@ -204,11 +205,11 @@ int pd_attn_prefill(const pd_attn_desc* desc, const pd_batch* batch, const void*
 int pd_attn_mixed(const pd_attn_desc* desc, const pd_batch* batch, const void* q, const void* k_pool,
                   const void* v_pool, void* o, float* lse, void* workspace, size_t workspace_bytes,
                   int32_t* dev_status, void* stream) {
-  (void)q; (void)k_pool; (void)v_pool; (void)o; (void)lse; (void)workspace; (void)workspace_bytes;
-  (void)dev_status; (void)stream;
-  const int rc = check_attn(desc, batch, true);
-  if (rc != PD_OK) return rc;
-  return PD_ERR_UNSUPPORTED;
+  // One launch of the persistent tensor-core kernel over the whole batch: each
+  // decode request (qo_len = 1) is a one-row query tile in the same
+  // heaviest-first work list as the prefill tiles, so prefill and decode work
+  // share the grid, the TMA pipeline and the MMA/softmax warps.
+  return pd_attn_prefill(desc, batch, q, k_pool, v_pool, o, lse, workspace, workspace_bytes, dev_status, stream);
 }
 
 namespace {

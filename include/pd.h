@@ -197,10 +197,14 @@ PD_API int pd_attn_prefill(const pd_attn_desc *desc, const pd_batch *batch, cons
                     void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
- * Mixed batch in one launch: requests with qo_len = 1 take the split-KV decode
- * path, the others the prefill path (section "Prefill vs Decode performance":
- * mixing prefill into decode batches). Arguments and support as
- * pd_attn_prefill.
+ * Mixed batch in one launch (section "Prefill vs Decode performance": mixing
+ * prefill into decode batches). Prefill requests (qo_len > 1) and decode
+ * requests (qo_len = 1) go through one persistent tensor-core kernel: every
+ * request's query rows are cut into 128-row tiles (a decode request is a
+ * one-row tile) and all tiles form one work list ordered by decreasing KV
+ * length, so both kinds of work share the grid and the TMA/MMA pipeline.
+ * Arguments, layouts and support as pd_attn_prefill; the workspace is that of
+ * pd_attn_workspace_size(kind = PD_KIND_MIXED).
  */
 PD_API int pd_attn_mixed(const pd_attn_desc *desc, const pd_batch *batch, const void *q,
                   const void *k_pool, const void *v_pool, void *o, float *lse,
