@@ -447,6 +447,43 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def profile_row(name: str, reps: int) -> None:
+    """Runs one hot-path call `reps` times on its workload (for ncu captures)."""
+    import torch
+    import decode_ragged_paged_gb300 as pd
+    from workloads import torch_gen
+    pd.load_library()
+    if name == "decode":
+        w = torch_gen.decode_batch()
+        fn = lambda: pd.pd_attn_decode(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
+                                       w["page_indices"], max_kv_len=4096)
+    elif name in ("prefill", "append"):
+        w = torch_gen.causal_prefill()
+        if name == "prefill":
+            fn = lambda: pd.pd_attn_prefill(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
+                                            w["page_indices"], w["qo_indptr"], max_qo_len=512, max_kv_len=512)
+        else:
+            fn = lambda: pd.pd_kv_append(w["k_new"], w["v_new"], w["k_pool"], w["v_pool"], w["qo_indptr"],
+                                         w["kv_len"], w["page_indptr"], w["page_indices"], max_kv_len=512)
+    elif name == "mixed":
+        w = torch_gen.mixed_1p_nd()
+        fn = lambda: pd.pd_attn_mixed(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
+                                      w["page_indices"], w["qo_indptr"], max_qo_len=1024, max_kv_len=1024)
+    elif name in ("pack", "unpack"):
+        w = torch_gen.kv_handoff()
+        if name == "pack":
+            fn = lambda: pd.pd_kv_pack(w["k_src"], w["v_src"], w["kv_len"], w["src_indptr"], w["src_indices"],
+                                       w["buffer"], w["offsets"], max_kv_len=512)
+        else:
+            fn = lambda: pd.pd_kv_unpack(w["buffer"], w["offsets"], w["k_dst"], w["v_dst"], w["kv_len"],
+                                         w["dst_indptr"], w["dst_indices"], max_kv_len=512)
+    else:
+        raise SystemExit(f"unknown row {name}")
+    for _ in range(reps):
+        fn()
+    torch.cuda.synchronize()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -457,7 +494,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile-row", default=None,
+                    help="run only this row's call (decode, append, prefill, mixed, pack, unpack) for ncu")
+    ap.add_argument("--profile-reps", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_row:
+        profile_row(args.profile_row, args.profile_reps)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
