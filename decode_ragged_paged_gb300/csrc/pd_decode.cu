@@ -14,7 +14,7 @@
 //              sharing one KV head, KV chunk) a producer warp streams the
 //              chunk's K then V page slices (contiguous runs in the HND layout)
 //              into a shared-memory ring with bulk async copies (TMA engine),
-//              and four consumer warps compute the scores, the chunk softmax and
+//              and the consumer warps compute the scores, the chunk softmax and
 //              the weighted value sum in fp32;
 //   3. merge   chunks of one request are combined by their log-sum-exp.
 #include <math.h>

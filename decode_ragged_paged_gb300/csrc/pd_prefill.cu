@@ -9,16 +9,18 @@
 //
 // One persistent CTA per SM walks a list of (request, 128-row q tile, query
 // head) items, heaviest first. Warp roles:
-//   warp 0    TMA producer: Q tile (double buffered), then K and V tiles of 128
-//             tokens (2-slot rings), each tile as one 128-byte-swizzled box per
-//             page and 64-column half; boxes past the request's pages are
-//             fetched out of range and arrive as zeros;
+//   warp 0    TMA producer of Q tiles (double buffered) and K tiles (2-slot
+//             ring), each tile one 128-byte-swizzled box per page and 64-column
+//             half; boxes past the request's pages are fetched out of range
+//             and arrive as zeros;
+//   warp 6    TMA producer of V tiles (2-slot ring), same boxes;
 //   warp 1    allocates 512 TMEM columns and issues tcgen05.mma:
-//             S = Q K^T into one of two S buffers, O += P V into the O buffer;
-//   warps 2-5 one query row per thread: online softmax on S read from TMEM,
-//             P (bf16) written to a swizzled shared tile for the P V product,
-//             O rescaled in TMEM only when the running max grows by more than
-//             2^8, final O / l and log-sum-exp written out.
+//             S = Q K^T into one of three S buffers, O += P V into the O
+//             buffer with P read from tensor memory;
+//   warps 2-5 one query row per thread: one-pass online softmax on S read from
+//             TMEM, P written back over S as bf16 pairs, O rescaled in TMEM
+//             only when the running max grows by more than 2^8, final O / l
+//             staged in shared memory and stored by TMA, log-sum-exp written.
 // Every wait is bounded; on a timeout the CTA records PD_DEV_TIMEOUT, drains
 // and frees its TMEM.
 #include <math.h>
