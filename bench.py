@@ -6,7 +6,7 @@
 Headline (one JSON line on rank 0): decode attention HBM throughput of the
 decode-batch workload (128 requests, qo_len 1, kv_len U[512, 4096], GQA 32/8,
 head_dim 128, page 16, bf16). A step is one pd_attn_decode call over the batch
-(plan, split-KV decode, merge). `value` = algorithmic bytes (K/V of every
+(plan, then split-KV decode with the merge of split partials fused in). `value` = algorithmic bytes (K/V of every
 cached token, q, o, lse and the page table) of all ranks / slowest rank's
 device time. The KV pools (1.14 GB) exceed the 126 MB L2, so no flush is
 needed between steps. `roofline` reports the split-KV decode kernel alone
@@ -255,14 +255,14 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (1.14 GB of KV pages); no flush between steps",
-                   "step": "one pd_attn_decode call: plan + split-KV decode + merge"},
+                   "step": "one pd_attn_decode call: plan + split-KV decode (merge fused)"},
         "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": round(achieved, 1),
                      "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
                      "peak_source": peaks["source"], "traffic": profiled_traffic("decode_kernel"),
                      "algorithmic_bytes": step_bytes, "kernel_ms": round(kernel_ms, 5)},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 2 * K,
         "clocks": clocks,
         "cpu_baseline": cpu,
         "rows": rows,
@@ -271,30 +271,36 @@ def run_ours(args):
 
 
 def timed(fn, reps, warm, flush=None, prof=True):
-    """Median device time (ms) of fn and of its main kernel (profiling events)."""
+    """Median device time (ms) of fn, of its main kernel (profiling events),
+    and the median host time (us) of one call. Every rep is enqueued back to
+    back (L2 flush, start event, call, end event) and the stream is
+    synchronised once at the end, so the host-side marshalling of a call
+    overlaps the device work queued before it and the events time the device."""
     import torch
     import decode_ragged_paged_gb300 as pd
     for _ in range(warm):
         fn()
-    tot, ker = [], []
+    torch.cuda.synchronize()
+    evs, host = [], []
     for _ in range(reps):
         if flush is not None:
             flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ka, kb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ka.record()
-        kb.record()
-        torch.cuda.synchronize()
+        a, b, ka, kb = (torch.cuda.Event(enable_timing=True) for _ in range(4))
         if prof:
+            ka.record()  # torch creates the CUDA event on its first record
+            kb.record()
             pd.pd_profile_events(ka, kb)
         a.record()
+        t0 = time.perf_counter()
         fn()
+        host.append(time.perf_counter() - t0)
         b.record()
         pd.pd_profile_events(None, None)
-        torch.cuda.synchronize()
-        tot.append(a.elapsed_time(b))
-        ker.append(ka.elapsed_time(kb) if prof else tot[-1])
-    return float(np.median(tot)), float(np.median(ker))
+        evs.append((a, b, ka, kb))
+    torch.cuda.synchronize()
+    tot = [a.elapsed_time(b) for a, b, _, _ in evs]
+    ker = [ka.elapsed_time(kb) for _, _, ka, kb in evs] if prof else tot
+    return float(np.median(tot)), float(np.median(ker)), float(np.median(host)) * 1e6
 
 
 def measure_rows(args, dev, peaks) -> dict:
@@ -311,10 +317,11 @@ def measure_rows(args, dev, peaks) -> dict:
     # causal prefill workload: append of its 4096 new tokens, then attention
     w = torch_gen.causal_prefill(device=dev)
     byts = 4 * w["k_new"].numel() * 2
-    ms, kms = timed(lambda: pd.pd_kv_append(w["k_new"], w["v_new"], w["k_pool"], w["v_pool"], w["qo_indptr"],
+    ms, kms, hus = timed(lambda: pd.pd_kv_append(w["k_new"], w["v_new"], w["k_pool"], w["v_pool"], w["qo_indptr"],
                                             w["kv_len"], w["page_indptr"], w["page_indices"], max_kv_len=512),
                     reps, warm, flush)
     rows["append"] = {"workload": "8 x 512 new tokens, 40 kv heads, D 128, page 16, bf16", "ms": round(ms, 5),
+                      "kernel_ms": round(kms, 5), "host_us": round(hus, 1),
                       "GBs": round(byts / kms / 1e6, 1), "frac_hbm": round(byts / kms / 1e6 / hbm, 4),
                       "bound": "hbm", "bytes": byts}
     L, H, B = 512, 40, 8
@@ -322,11 +329,13 @@ def measure_rows(args, dev, peaks) -> dict:
     pf_bytes = 4 * w["q"].numel() * 2
     try:
         o = torch.empty_like(w["q"])
-        ms, kms = timed(lambda: pd.pd_attn_prefill(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
+        ms, kms, hus = timed(lambda: pd.pd_attn_prefill(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
                                                    w["page_indices"], w["qo_indptr"], max_qo_len=512,
                                                    max_kv_len=512, o=o), reps, warm, flush)
         t = flops / (kms * 1e-3) / 1e12
         rows["prefill"] = {"workload": "8 x 512 causal, 40 heads, D 128, page 16, bf16", "ms": round(ms, 5),
+                           "kernel_ms": round(kms, 5), "host_us": round(hus, 1),
+                           "call_TFLOPs": round(flops / (ms * 1e-3) / 1e12, 1),
                            "TFLOPs": round(t, 1), "frac_bf16": round(t / peaks["bf16"], 4),
                            "GBs": round(pf_bytes / kms / 1e6, 1), "frac_hbm": round(pf_bytes / kms / 1e6 / hbm, 4),
                            "bound": "hbm (128 flop/B < ridge)", "flops": flops, "bytes": pf_bytes}
@@ -341,7 +350,7 @@ def measure_rows(args, dev, peaks) -> dict:
     mflops = 2 * 128 * pre * (pre + 1) * 40 + 4 * 128 * int(w["kv_len_host"][1:].sum()) * 40
     try:
         o = torch.empty_like(w["q"])
-        ms, kms = timed(lambda: pd.pd_attn_mixed(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
+        ms, kms, hus = timed(lambda: pd.pd_attn_mixed(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
                                                  w["page_indices"], w["qo_indptr"], max_qo_len=1024,
                                                  max_kv_len=1024, o=o), reps, warm, flush)
         o_p, o_d = o[:pre], o[pre:]
@@ -352,12 +361,13 @@ def measure_rows(args, dev, peaks) -> dict:
             pd.pd_attn_decode(w["q"][pre:], w["k_pool"], w["v_pool"], w["kv_len"][1:], w["page_indptr"][1:],
                               w["page_indices"], max_kv_len=576, o=o_d)
 
-        sep_ms, _ = timed(separate, reps, warm, flush, prof=False)
-        dec_ms, dec_kms = timed(lambda: pd.pd_attn_decode(w["q"][pre:], w["k_pool"], w["v_pool"], w["kv_len"][1:],
+        sep_ms, _, _ = timed(separate, reps, warm, flush, prof=False)
+        dec_ms, dec_kms, _ = timed(lambda: pd.pd_attn_decode(w["q"][pre:], w["k_pool"], w["v_pool"], w["kv_len"][1:],
                                                           w["page_indptr"][1:], w["page_indices"], max_kv_len=576,
                                                           o=o_d), reps, warm, flush)
         rows["mixed"] = {"workload": "1 prefill (1024) + 63 decodes (kv U[512,576]), 40 heads, D 128, bf16",
-                         "fused_ms": round(ms, 5), "fused_kernel_ms": round(kms, 5),
+                         "fused_ms": round(ms, 5), "fused_kernel_ms": round(kms, 5), "host_us": round(hus, 1),
+                         "call_GBs": round(kvb / ms / 1e6, 1),
                          "GBs": round(kvb / kms / 1e6, 1), "frac_hbm": round(kvb / kms / 1e6 / hbm, 4),
                          "TFLOPs": round(mflops / kms / 1e9, 1), "bound": "hbm", "bytes": kvb, "flops": mflops,
                          "separate_ms": round(sep_ms, 5), "decode_only_ms": round(dec_ms, 5),
@@ -370,14 +380,16 @@ def measure_rows(args, dev, peaks) -> dict:
 
     w = torch_gen.kv_handoff(device=dev)
     byts = 2 * w["buffer"].numel()
-    ms, kms = timed(lambda: pd.pd_kv_pack(w["k_src"], w["v_src"], w["kv_len"], w["src_indptr"], w["src_indices"],
+    ms, kms, hus = timed(lambda: pd.pd_kv_pack(w["k_src"], w["v_src"], w["kv_len"], w["src_indptr"], w["src_indices"],
                                           w["buffer"], w["offsets"], max_kv_len=512), reps, warm)
     rows["pack"] = {"workload": "8 req x 512 tok x 40 layers x 40 kv heads x 128, bf16, page 16",
-                    "ms": round(ms, 5), "GBs": round(byts / kms / 1e6, 1), "frac_hbm": round(byts / kms / 1e6 / hbm, 4),
+                    "ms": round(ms, 5), "kernel_ms": round(kms, 5), "host_us": round(hus, 1),
+                    "GBs": round(byts / kms / 1e6, 1), "frac_hbm": round(byts / kms / 1e6 / hbm, 4),
                     "bound": "hbm", "bytes": byts}
-    ms, kms = timed(lambda: pd.pd_kv_unpack(w["buffer"], w["offsets"], w["k_dst"], w["v_dst"], w["kv_len"],
+    ms, kms, hus = timed(lambda: pd.pd_kv_unpack(w["buffer"], w["offsets"], w["k_dst"], w["v_dst"], w["kv_len"],
                                             w["dst_indptr"], w["dst_indices"], max_kv_len=512), reps, warm)
     rows["unpack"] = {"workload": "same buffers into a page-64 pool with its own table", "ms": round(ms, 5),
+                      "kernel_ms": round(kms, 5), "host_us": round(hus, 1),
                       "GBs": round(byts / kms / 1e6, 1), "frac_hbm": round(byts / kms / 1e6 / hbm, 4),
                       "bound": "hbm", "bytes": byts}
     del w

@@ -20,6 +20,15 @@ __device__ __forceinline__ void report(int32_t* status, int32_t code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// Programmatic dependent launch: a primary grid lets the next kernel on the
+// stream (launched with programmatic stream serialisation) start its
+// prologue; the dependent waits for the primary's completion and memory
+// before touching the primary's results. Both are no-ops without such a launch.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -7,9 +7,11 @@
 // applied here to the KV axis). Section "Qwen3-Coder": grouped-query attention,
 // so one KV head serves several query heads.
 //
-// Three launches on the caller's stream:
+// Three launches on the caller's stream, each a programmatic dependent of the
+// one before:
 //   1. plan    one CTA validates lengths and tables, cuts every request's KV
-//              into equal chunks and writes the work list into the workspace;
+//              into equal chunks and writes the work list, longest chunks
+//              first, into the workspace;
 //   2. decode  persistent CTAs; per work item (request, group of query heads
 //              sharing one KV head, KV chunk) a producer warp streams the
 //              chunk's K then V page slices (contiguous runs in the HND layout)
@@ -179,6 +181,16 @@ __device__ __forceinline__ Item decode_item(const DecodeParams& p, int it) {
   return I;
 }
 
+// Item of CTA b in hand-out round k: rounds alternate direction over the
+// grid, so with items sorted longest first each CTA's total stays close to the
+// mean.
+#ifndef PD_DECODE_SERPENTINE
+#define PD_DECODE_SERPENTINE 1
+#endif
+__device__ __forceinline__ int serpentine_item(int k, int b, int grid) {
+  return k * grid + ((PD_DECODE_SERPENTINE && (k & 1)) ? grid - 1 - b : b);
+}
+
 __device__ __forceinline__ bool consumer_sync(uint64_t* bar, uint32_t& phase, int lane,
                                               volatile int* abort, int32_t* status) {
   __syncwarp();
@@ -192,13 +204,24 @@ __device__ __forceinline__ bool consumer_sync(uint64_t* bar, uint32_t& phase, in
 
 // ------------------------------------------------------------------- plan
 // One CTA. Per request: validate, choose the chunk length (equal chunks of at
-// most chunk_target tokens, multiples of the stage size), then scan the chunk
-// counts and write the (request, chunk) list.
+// most chunk_target tokens, multiples of the stage size), scan the chunk
+// counts (each chunk's slot for its partial result) and give requests without
+// keys their final o = 0, lse = -inf. Then list the
+// (request, chunk) pairs longest first (counting sort on the stage count), so
+// that the decode kernel's serpentine hand-out balances the CTAs.
+#ifndef PD_DECODE_SORT
+#define PD_DECODE_SORT 1
+#endif
+constexpr int kLenBuckets = kMaxChunk / kTS;  // chunk lengths in stages: 1 .. kLenBuckets
+
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p) {
+  pdl_launch_dependents();
   __shared__ int warp_sums[32];
   __shared__ int carry;
+  __shared__ int bucket_cnt[kLenBuckets + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) carry = 0;
+  if (tid <= kLenBuckets) bucket_cnt[tid] = 0;
   __syncthreads();
   for (int base = 0; base < p.batch; base += blockDim.x) {
     const int r = base + tid;
@@ -227,6 +250,10 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
         clen = (n + n_c - 1) / n_c;
         clen = (clen + kTS - 1) / kTS * kTS;
         n_c = (n + clen - 1) / clen;
+        const int last = n - (n_c - 1) * clen;
+        const int full = last == clen ? n_c : n_c - 1;
+        if (full > 0) atomicAdd(&bucket_cnt[clen / kTS], full);
+        if (last != clen) atomicAdd(&bucket_cnt[(last + kTS - 1) / kTS], 1);
       }
     }
     // block-wide exclusive scan of n_c
@@ -249,13 +276,49 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
     }
     __syncthreads();
     const int excl = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + x - n_c;
-    if (r < p.batch) {
-      p.req_info[r] = make_int4(excl, n_c, clen, row);
-      for (int c = 0; c < n_c; ++c) p.rc_list[excl + c] = make_int2(r, c);
-    }
+    if (r < p.batch) p.req_info[r] = make_int4(excl, n_c, clen, row);
     __syncthreads();
     if (tid == 0) carry += warp_sums[(blockDim.x >> 5) - 1];
     __syncthreads();
+  }
+  // bucket starts, longest chunks first (bucket_cnt becomes a cursor)
+  if (tid == 0) {
+    int pos = 0;
+    for (int b = kLenBuckets; b >= 1; --b) {
+      const int c = bucket_cnt[b];
+      bucket_cnt[b] = pos;
+      pos += c;
+    }
+  }
+  __syncthreads();
+  for (int r = tid; r < p.batch; r += blockDim.x) {
+    const int4 info = p.req_info[r];
+    if (info.w < 0) continue;
+    if (info.y == 0) {
+      // no keys: final output now (the decode kernel never sees this request)
+      for (int k = 0; k < p.hq * p.head_dim; ++k) {
+        const int64_t off = (int64_t)info.w * p.hq * p.head_dim + k;
+        if (p.o_dtype == PD_BF16)
+          static_cast<uint16_t*>(p.o)[off] = 0;
+        else
+          static_cast<float*>(p.o)[off] = 0.f;
+      }
+      if (p.lse != nullptr)
+        for (int h = 0; h < p.hq; ++h) p.lse[(int64_t)info.w * p.hq + h] = -INFINITY;
+      continue;
+    }
+    const int n = p.kv_len[r], clen = info.z, n_c = info.y;
+    if (!PD_DECODE_SORT) {
+      for (int c = 0; c < n_c; ++c) p.rc_list[info.x + c] = make_int2(r, c);
+      continue;
+    }
+    const int last = n - (n_c - 1) * clen;
+    const int full = last == clen ? n_c : n_c - 1;
+    if (full > 0) {
+      const int q = atomicAdd(&bucket_cnt[clen / kTS], full);
+      for (int c = 0; c < full; ++c) p.rc_list[q + c] = make_int2(r, c);
+    }
+    if (last != clen) p.rc_list[atomicAdd(&bucket_cnt[(last + kTS - 1) / kTS], 1)] = make_int2(r, n_c - 1);
   }
   if (tid == 0) {
     p.hdr[1] = carry;
@@ -295,6 +358,8 @@ __global__ void __launch_bounds__(kThreads, PD_DECODE_MIN_BLOCKS) decode_kernel(
     fence_barrier_init();
   }
   __syncthreads();
+  pdl_wait_primary();  // the plan kernel's list, counters and lengths
+  pdl_launch_dependents();
 
   const int n_items = p.hdr[0];
 
@@ -308,7 +373,9 @@ __global__ void __launch_bounds__(kThreads, PD_DECODE_MIN_BLOCKS) decode_kernel(
       const uint64_t policy = make_evict_first();
       const uint8_t* kpool = static_cast<const uint8_t*>(p.k_pool);
       const uint8_t* vpool = static_cast<const uint8_t*>(p.v_pool);
-      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+      for (int k = 0;; ++k) {
+        const int it = serpentine_item(k, blockIdx.x, gridDim.x);
+        if (it >= n_items) break;
         const Item I = decode_item(p, it);
         if (I.q_row < 0) continue;
         const int32_t* pages = p.page_indices + p.page_indptr[I.r];
@@ -353,7 +420,9 @@ __global__ void __launch_bounds__(kThreads, PD_DECODE_MIN_BLOCKS) decode_kernel(
     const int cw = warp;
     const int tg = lane >> 3, dg = lane & 7;
     uint32_t ctr = 0, sync_phase = 0;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    for (int k = 0;; ++k) {
+      const int it = serpentine_item(k, blockIdx.x, gridDim.x);
+      if (it >= n_items) break;
       const Item I = decode_item(p, it);
       if (I.q_row < 0) continue;
       const int n_tok = I.t_end - I.t_begin;
@@ -518,51 +587,76 @@ __global__ void __launch_bounds__(kThreads, PD_DECODE_MIN_BLOCKS) decode_kernel(
 }
 
 // ------------------------------------------------------------------ merge
-// One warp per (request, query head): combine the chunks' partial outputs by
-// their log-sum-exp; requests with no key get o = 0 and lse = -inf.
+// One warp per (request, query head) of a request split into several chunks:
+// combine the chunks' partial outputs by their log-sum-exp. Each lane owns
+// D / 32 consecutive dimensions; four chunks' loads are in flight at a time.
 template <int D>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
+  pdl_wait_primary();  // the decode kernel's partials
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= p.batch * p.hq) return;
   const int r = gw / p.hq, h = gw % p.hq;
   const int4 info = p.req_info[r];
-  if (info.w < 0 || info.y == 1) return;
-  const int64_t orow = ((int64_t)info.w * p.hq + h) * D;
+  if (info.w < 0 || info.y <= 1) return;
   constexpr int PER = D / 32;
-  float out[PER];
-  float lse_nat;
-  if (info.y == 0) {
+  static_assert(PER == 2 || PER == 4, "head_dim 64 or 128");
+  const int n = info.y;
+  const float* pl = p.part_lse + (int64_t)info.x * p.hq + h;
+  float m = -INFINITY;
+  for (int c = lane; c < n; c += 32) m = fmaxf(m, __ldcg(pl + (int64_t)c * p.hq));
 #pragma unroll
-    for (int k = 0; k < PER; ++k) out[k] = 0.f;
-    lse_nat = -INFINITY;
-  } else {
-    float m = -INFINITY;
-    for (int c = lane; c < info.y; c += 32) m = fmaxf(m, p.part_lse[(int64_t)(info.x + c) * p.hq + h]);
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  float l = 0.f;
+  for (int c = lane; c < n; c += 32) l += exp2f(__ldcg(pl + (int64_t)c * p.hq) - m);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
+  const float* po = p.part_o + ((int64_t)info.x * p.hq + h) * D + lane * PER;
+  const int64_t cs = (int64_t)p.hq * D;  // chunk stride of part_o
+  float acc[PER];
 #pragma unroll
-    for (int k = 0; k < PER; ++k) out[k] = 0.f;
-    float wsum = 0.f;
-    for (int c = 0; c < info.y; ++c) {
-      const int64_t pc = (int64_t)(info.x + c) * p.hq + h;
-      const float w = exp2f(p.part_lse[pc] - m);
-      wsum += w;
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  auto load = [&](int c, float (&v)[PER]) {
+    if constexpr (PER == 4) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(po + c * cs));
+      v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w;
+    } else {
+      const float2 x = __ldcg(reinterpret_cast<const float2*>(po + c * cs));
+      v[0] = x.x, v[1] = x.y;
+    }
+  };
+  int c = 0;
+  for (; c + 4 <= n; c += 4) {
+    float lw[4], v[4][PER];
 #pragma unroll
-      for (int k = 0; k < PER; ++k) out[k] = fmaf(w, p.part_o[pc * D + lane + 32 * k], out[k]);
+    for (int j = 0; j < 4; ++j) {
+      lw[j] = __ldcg(pl + (int64_t)(c + j) * p.hq);
+      load(c + j, v[j]);
     }
 #pragma unroll
-    for (int k = 0; k < PER; ++k) out[k] /= wsum;
-    lse_nat = (m + log2f(wsum)) * kLn2;
-  }
+    for (int j = 0; j < 4; ++j) {
+      const float w = exp2f(lw[j] - m);
 #pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    if (p.o_dtype == PD_BF16)
-      static_cast<uint16_t*>(p.o)[orow + lane + 32 * k] = f32_to_bf16_bits(out[k]);
-    else
-      static_cast<float*>(p.o)[orow + lane + 32 * k] = out[k];
+      for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, v[j][e], acc[e]);
+    }
   }
-  if (lane == 0 && p.lse != nullptr) p.lse[(int64_t)info.w * p.hq + h] = lse_nat;
+  for (; c < n; ++c) {
+    float v[PER];
+    load(c, v);
+    const float w = exp2f(__ldcg(pl + (int64_t)c * p.hq) - m);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+  }
+  const float inv = 1.f / l;
+  const int64_t orow = ((int64_t)info.w * p.hq + h) * D + lane * PER;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    if (p.o_dtype == PD_BF16)
+      static_cast<uint16_t*>(p.o)[orow + e] = f32_to_bf16_bits(acc[e] * inv);
+    else
+      static_cast<float*>(p.o)[orow + e] = acc[e] * inv;
+  }
+  if (lane == 0 && p.lse != nullptr) p.lse[(int64_t)info.w * p.hq + h] = (m + log2f(l)) * kLn2;
 }
 
 // ------------------------------------------------------------------- host
@@ -603,6 +697,23 @@ DecodeLayout decode_layout(int32_t batch, int32_t hq, int32_t head_dim, int32_t 
 
 namespace {
 
+// Launch with programmatic stream serialisation when `pdl` is set.
+template <typename Kernel>
+cudaError_t launch_dependent(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                             const DecodeParams& p) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 template <int ES, int D, int GS>
 int run_decode(DecodeParams& p, cudaStream_t stream) {
   constexpr size_t smem = decode_smem_bytes<ES, D, GS>();
@@ -625,11 +736,20 @@ int run_decode(DecodeParams& p, cudaStream_t stream) {
   int64_t grid = (int64_t)device_sm_count() * blocks_per_sm;
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
+  // Each kernel is a programmatic dependent of the previous one: its CTAs are
+  // placed and set up while the previous kernel drains. When the decode kernel
+  // is timed alone (profiling events) it runs without that overlap.
+  const bool timed = profile_events().start != nullptr;
   profile_begin(stream);
-  decode_kernel<ES, D, GS><<<(unsigned)grid, kThreads, smem, stream>>>(p);
+  if (launch_dependent(decode_kernel<ES, D, GS>, dim3((unsigned)grid), dim3(kThreads), smem, stream, !timed, p) !=
+      cudaSuccess)
+    return PD_ERR_CUDA;
   profile_end(stream);
   const int warps = p.batch * p.hq;
-  if (warps > 0) decode_merge_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(p);
+  if (warps > 0 &&
+      launch_dependent(decode_merge_kernel<D>, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, stream, !timed, p) !=
+          cudaSuccess)
+    return PD_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
 }
 

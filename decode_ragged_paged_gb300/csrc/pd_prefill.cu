@@ -14,9 +14,11 @@
 //             half; boxes past the request's pages are fetched out of range
 //             and arrive as zeros;
 //   warp 6    TMA producer of V tiles (2-slot ring), same boxes;
-//   warp 1    allocates 512 TMEM columns and issues tcgen05.mma:
-//             S = Q K^T into one of three S buffers, O += P V into the O
-//             buffer with P read from tensor memory;
+//   warp 1    allocates 512 TMEM columns and issues S = Q K^T (tcgen05.mma)
+//             into one of three S buffers;
+//   warp 7    issues O += P V into the O buffer with P read from tensor
+//             memory (two issuing warps: one thread's tcgen05.mma issue rate
+//             and commits limited a single issuer);
 //   warps 2-5 one query row per thread: one-pass online softmax on S read from
 //             TMEM, P written back over S as bf16 pairs, O rescaled in TMEM
 //             only when the running max grows by more than 2^8, final O / l
@@ -37,8 +39,9 @@ namespace {
 constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per tile
 constexpr int kD = 128;           // head_dim
-constexpr int kThreadsPf = 224;   // 7 warps: Q/K loads, MMA, 4 softmax, V loads
+constexpr int kThreadsPf = 256;   // 8 warps: Q/K loads, S MMA, 4 softmax, V loads, P V MMA
 constexpr int kWarpV = 6;         // the warp that loads V tiles
+constexpr int kWarpPV = 7;        // the warp that issues O += P V
 constexpr uint32_t kTileBytes = kBM * kD * 2;  // one bf16 128 x 128 tile
 constexpr uint32_t kHalf = kTileBytes / 2;     // one 64-column half: 128 rows x 128 B
 constexpr uint32_t kTmemCols = 512;
@@ -50,15 +53,25 @@ constexpr int kBuckets = 1024;
 
 // shared-memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t kOffQ = 0;                  // 2 tiles
-constexpr uint32_t kOffK = 2 * kTileBytes;     // 2 tiles
-constexpr uint32_t kOffV = 4 * kTileBytes;     // 2 tiles
-constexpr uint32_t kOffO = 6 * kTileBytes;     // 1 tile: bf16 O staged for the TMA store
+// K and V ring depths (five tiles between them; a full bf16 O tile is staged
+// in its item's Q buffer)
+#ifndef PD_PREFILL_K_SLOTS
+#define PD_PREFILL_K_SLOTS 3
+#endif
+#ifndef PD_PREFILL_V_SLOTS
+#define PD_PREFILL_V_SLOTS (5 - PD_PREFILL_K_SLOTS)
+#endif
+constexpr int kKSlots = PD_PREFILL_K_SLOTS;
+constexpr int kVSlots = PD_PREFILL_V_SLOTS;
+static_assert(kKSlots >= 2 && kVSlots >= 2 && kKSlots + kVSlots <= 5, "ring depths");
+constexpr uint32_t kOffK = 2 * kTileBytes;
+constexpr uint32_t kOffV = (2 + kKSlots) * kTileBytes;
 constexpr uint32_t kOffBar = 7 * kTileBytes;
 constexpr size_t kPrefillSmem = 7 * kTileBytes + 256 + 1024;
 
 struct Bars {
-  uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[kSB], s_empty[kSB], p_full[kSB], pv_done[kSB], drain, o_sync;
+  uint64_t q_full[2], q_empty[2], k_full[kKSlots], v_full[kVSlots];
+  uint64_t s_full[kSB], p_full[kSB], pv_done[kSB], drain, o_sync;
   uint32_t tmem_slot;
   int abort;
 };
@@ -97,6 +110,14 @@ __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int it) {
   return I;
 }
 
+// The item after the current one is read while the current one is worked on,
+// so the dependent loads of its description leave the critical path.
+__device__ __forceinline__ PItem prefill_item_or_empty(const PrefillParams& p, int it, int n_items) {
+  if (it < n_items) return prefill_item(p, it);
+  PItem I{};
+  return I;
+}
+
 __device__ __forceinline__ bool request_ok(const PrefillParams& p, int r) {
   const int a = p.qo_indptr[r], b = p.qo_indptr[r + 1];
   const int n = p.kv_len[r];
@@ -112,30 +133,42 @@ __device__ __forceinline__ bool request_ok(const PrefillParams& p, int r) {
   return code == 0;
 }
 
-// Loads one 128-token K or V tile: per 64-column half, one box per page (or one
-// box of 128 slots when a page holds at least 128 tokens).
-__device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const PItem& I, int j, const CUtensorMap* map,
-                                             uint8_t* dst, uint64_t* bar, int lane) {
+// Boxes of one 128-token K or V tile: per 64-column half, one box per page (or
+// one box of 128 slots when a page holds at least 128 tokens). Lane l < boxes
+// finds its box's page and slot offset; pages past the request's end (and bad
+// ids) map to num_pages, which the TMA unit fetches as zeros.
+struct TileBox {
+  int pid, soff;
+};
+
+__device__ __forceinline__ TileBox tile_box(const PrefillParams& p, int pbase, int need, int j, int lane) {
   const int pb = p.page_size < kBN ? p.page_size : kBN;  // slots per box
   const int nb = kBN / pb;                                // boxes per half
-  const int t0 = j * kBN;
-  int pid = p.num_pages, soff = 0;                        // out of range: zero fill
+  TileBox t{p.num_pages, 0};
   if (lane < nb) {
-    const int pidx = (t0 + lane * pb) / p.page_size;
-    soff = (t0 + lane * pb) % p.page_size;
-    if (pidx < I.need) {
-      pid = __ldg(p.page_indices + I.pbase + pidx);
-      if (pid < 0 || pid >= p.num_pages) {
+    const int tok = j * kBN + lane * pb;
+    const int pidx = tok / p.page_size;
+    t.soff = tok % p.page_size;
+    if (pidx < need) {
+      t.pid = __ldg(p.page_indices + pbase + pidx);
+      if (t.pid < 0 || t.pid >= p.num_pages) {
         report(p.status, PD_DEV_BAD_PAGE_TABLE);
-        pid = p.num_pages;
+        t.pid = p.num_pages;
       }
     }
   }
+  return t;
+}
+
+__device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const TileBox& t, const CUtensorMap* map,
+                                             int g, uint8_t* dst, uint64_t* bar, int lane) {
+  const int pb = p.page_size < kBN ? p.page_size : kBN;
+  const int nb = kBN / pb;
   if (lane == 0) mbar_arrive_expect_tx(bar, kTileBytes);
   __syncwarp();
   if (lane < nb) {
-    tma_load_4d(dst + lane * pb * 128, map, 0, soff, I.g, pid, bar);
-    tma_load_4d(dst + kHalf + lane * pb * 128, map, 64, soff, I.g, pid, bar);
+    tma_load_4d(dst + lane * pb * 128, map, 0, t.soff, g, t.pid, bar);
+    tma_load_4d(dst + kHalf + lane * pb * 128, map, 64, t.soff, g, t.pid, bar);
   }
 }
 
@@ -144,33 +177,63 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const PItem
 // ------------------------------------------------------------------- plan
 // One CTA: validate, then order the (request, q tile) pairs by decreasing
 // number of KV tiles (counting sort) so that the heaviest items start first.
+static_assert(kBuckets == 1024, "the plan kernel scans one bucket per thread of its 1024");
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams p) {
   __shared__ int hist[kBuckets];
   __shared__ int cursor[kBuckets];
+  pdl_launch_dependents();
   const int tid = threadIdx.x;
   for (int b = tid; b < kBuckets; b += blockDim.x) hist[b] = 0;
   __syncthreads();
+  // an entry covers one q tile, or two adjacent ones in pair mode (weighed by
+  // the KV tiles of its last tile, the heaviest of the two)
+  const int span = p.pair ? 2 : 1;
   for (int r = tid; r < p.batch; r += blockDim.x) {
     if (!request_ok(p, r)) continue;
     const int qo = p.qo_indptr[r + 1] - p.qo_indptr[r], n = p.kv_len[r];
-    for (int qt = 0; qt * kBM < qo; ++qt) atomicAdd(&hist[min(kv_tiles(qt, qo, n, p.causal), kBuckets - 1)], 1);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int b = kBuckets - 1; b >= 0; --b) {
-      cursor[b] = acc;
-      acc += hist[b];
+    const int tiles = (qo + kBM - 1) / kBM;
+    for (int e = 0; e * span < tiles; ++e) {
+      const int last = min(e * span + span, tiles) - 1;
+      atomicAdd(&hist[min(kv_tiles(last, qo, n, p.causal), kBuckets - 1)], 1);
     }
-    p.hdr[0] = min(acc, p.max_rq) * p.hq;
+  }
+  __syncthreads();
+  {
+    // exclusive scan over the buckets in decreasing order, one bucket per thread
+    __shared__ int warp_tot[32];
+    const int lane = tid & 31, warp = tid >> 5;
+    const int b = kBuckets - 1 - tid;
+    const int c = hist[b];
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_tot[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_tot[lane] = w;  // inclusive
+    }
+    __syncthreads();
+    cursor[b] = (warp > 0 ? warp_tot[warp - 1] : 0) + x - c;
+    if (tid == 0) p.hdr[0] = min(warp_tot[31], p.max_rq) * p.hq;
   }
   __syncthreads();
   for (int r = tid; r < p.batch; r += blockDim.x) {
     if (!request_ok(p, r)) continue;
     const int qo = p.qo_indptr[r + 1] - p.qo_indptr[r], n = p.kv_len[r];
-    for (int qt = 0; qt * kBM < qo; ++qt) {
-      const int pos = atomicAdd(&cursor[min(kv_tiles(qt, qo, n, p.causal), kBuckets - 1)], 1);
-      if (pos < p.max_rq) p.rq_list[pos] = make_int2(r, qt);
+    const int tiles = (qo + kBM - 1) / kBM;
+    for (int e = 0; e * span < tiles; ++e) {
+      const int last = min(e * span + span, tiles) - 1;
+      const int pos = atomicAdd(&cursor[min(kv_tiles(last, qo, n, p.causal), kBuckets - 1)], 1);
+      if (pos < p.max_rq) p.rq_list[pos] = make_int2(r, e);
     }
   }
 }
@@ -185,7 +248,6 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
   uint8_t* sQ = base + kOffQ;
   uint8_t* sK = base + kOffK;
   uint8_t* sV = base + kOffV;
-  uint8_t* sO = base + kOffO;
   Bars* bars = reinterpret_cast<Bars*>(base + kOffBar);
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -193,19 +255,17 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->q_full[i], 1);
-      mbar_init(&bars->q_empty[i], 1);
-      mbar_init(&bars->k_full[i], 1);
-      mbar_init(&bars->k_empty[i], 1);
-      mbar_init(&bars->v_full[i], 1);
-      mbar_init(&bars->v_empty[i], 1);
+      // the item's last S product, and the read of the O tile staged in it
+      mbar_init(&bars->q_empty[i], 2);
     }
+    for (int i = 0; i < kKSlots; ++i) mbar_init(&bars->k_full[i], 1);
+    for (int i = 0; i < kVSlots; ++i) mbar_init(&bars->v_full[i], 1);
     for (int i = 0; i < kSB; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_empty[i], 1);
       mbar_init(&bars->p_full[i], 4);
       mbar_init(&bars->pv_done[i], 1);
     }
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, 2);  // one commit from each MMA-issuing warp
     mbar_init(&bars->o_sync, 4);
     bars->abort = 0;
     fence_barrier_init();
@@ -223,6 +283,7 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
+  pdl_wait_primary();  // the plan kernel's item list
   const int n_items = p.hdr[0];
 
   if (warp == 0 || warp == kWarpV) {
@@ -232,8 +293,10 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
     // double the rate at which a tile's page boxes are requested.
     const bool is_v = warp == kWarpV;
     uint32_t it_ctr = 0, kv_ctr = 0;
+    PItem nxt = prefill_item_or_empty(p, blockIdx.x, n_items);
     for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++it_ctr) {
-      const PItem I = prefill_item(p, it);
+      const PItem I = nxt;
+      nxt = prefill_item_or_empty(p, it + gridDim.x, n_items);
       if (!is_v) {
         const int qb = it_ctr & 1;
         if (!warp_mbar_wait(&bars->q_empty[qb], ((it_ctr >> 1) & 1u) ^ 1u, abort, p.status)) break;
@@ -245,109 +308,122 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         __syncwarp();
       }
       bool ok = true;
+      const uint32_t depth = is_v ? (uint32_t)kVSlots : (uint32_t)kKSlots;
       for (int j = 0; j < I.n_kv && ok; ++j, ++kv_ctr) {
-        const int slot = kv_ctr & 1;
-        const uint32_t par = ((kv_ctr >> 1) & 1u) ^ 1u;
-        if (!is_v) {
-          ok = warp_mbar_wait(&bars->k_empty[slot], par, abort, p.status);
-          if (ok) load_kv_tile(p, I, j, &tm_k, sK + slot * kTileBytes, &bars->k_full[slot], lane);
-        } else {
-          ok = warp_mbar_wait(&bars->v_empty[slot], par, abort, p.status);
-          if (ok) load_kv_tile(p, I, j, &tm_v, sV + slot * kTileBytes, &bars->v_full[slot], lane);
+        const int slot = kv_ctr % depth;
+        const TileBox box = tile_box(p, I.pbase, I.need, j, lane);  // page ids read before the slot wait
+        // The slot's previous tile u = kv_ctr - depth is done with it once S_u
+        // (for K) or P_u V_u (for V) has completed; every tile's phase is waited
+        // in order, so a parity wait is never more than one phase behind.
+        if (kv_ctr >= depth) {
+          const uint32_t u = kv_ctr - depth;
+          ok = warp_mbar_wait(is_v ? &bars->pv_done[u % kSB] : &bars->s_full[u % kSB], (u / kSB) & 1u, abort,
+                              p.status);
+        }
+        if (ok) {
+          if (!is_v)
+            load_kv_tile(p, box, &tm_k, I.g, sK + slot * kTileBytes, &bars->k_full[slot], lane);
+          else
+            load_kv_tile(p, box, &tm_v, I.g, sV + slot * kTileBytes, &bars->v_full[slot], lane);
         }
       }
       if (!ok) break;
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA
-    // S_j = Q K_j^T into TMEM buffer j % kSB; the softmax warps overwrite that
-    // buffer with P_j (bf16), which O += P_j V_j reads as its A operand; the
-    // buffer is free again once that product has completed.
+    // ------------------------------------------------------------- S = Q K^T
+    // S_j into TMEM buffer j % kSB, as soon as K_j has landed and the buffer's
+    // previous tile has gone through P V. The softmax warps overwrite S_j with
+    // P_j (bf16), which warp kWarpPV multiplies into O.
     constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, 1);
-    const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
-    uint32_t it_ctr = 0, kv_ctr = 0, s_ctr = 0, pv_ctr = 0;
+    const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK);
+    uint32_t it_ctr = 0, kv_ctr = 0;
     bool ok = true;
+    PItem nxt = prefill_item_or_empty(p, blockIdx.x, n_items);
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++it_ctr) {
-      const PItem I = prefill_item(p, it);
+      const PItem I = nxt;
+      nxt = prefill_item_or_empty(p, it + gridDim.x, n_items);
       const int qb = it_ctr & 1;
       ok = warp_mbar_wait(&bars->q_full[qb], (it_ctr >> 1) & 1u, abort, p.status);
       if (!ok) break;
       tc_fence_after();
-      int prev_slot = 0, prev_sb = 0;
-      uint32_t prev_par = 0;
-      for (int j = 0; j <= I.n_kv; ++j) {
-        int slot = 0, sb = 0;
-        uint32_t par = 0;
-        if (j < I.n_kv) {
-          slot = kv_ctr & 1;
-          par = (kv_ctr >> 1) & 1u;
-          sb = s_ctr % kSB;
-          ok = warp_mbar_wait(&bars->k_full[slot], par, abort, p.status) &&
-               warp_mbar_wait(&bars->s_empty[sb], ((s_ctr / kSB) & 1u) ^ 1u, abort, p.status);
-          if (!ok) break;
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t qa = sQa + qb * kTileBytes, ka = sKa + slot * kTileBytes;
+      const uint64_t dq = sw128_desc(sQa + qb * kTileBytes, 16, 1024);
+      for (int j = 0; j < I.n_kv; ++j, ++kv_ctr) {
+        const int slot = kv_ctr % kKSlots;
+        const int sb = kv_ctr % kSB;
+        // every tile's phase of pv_done is waited in order (tiles >= kSB)
+        ok = warp_mbar_wait(&bars->k_full[slot], (kv_ctr / kKSlots) & 1u, abort, p.status) &&
+             (kv_ctr < (uint32_t)kSB ||
+              warp_mbar_wait(&bars->pv_done[sb], ((kv_ctr - kSB) / kSB) & 1u, abort, p.status));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint64_t dk = sw128_desc(sKa + slot * kTileBytes, 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint32_t off = (kk / 4) * kHalf + (kk % 4) * 32;
-              tc_mma_f16(tmem + col_s(sb), sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024), idesc_s,
-                         kk > 0);
-            }
-            tc_commit(&bars->s_full[sb]);
-            tc_commit(&bars->k_empty[slot]);
-            if (j == I.n_kv - 1) tc_commit(&bars->q_empty[qb]);
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = (kk / 4) * kHalf + (kk % 4) * 32;
+            tc_mma_f16(tmem + col_s(sb), desc_advance(dq, off), desc_advance(dk, off), idesc_s, kk > 0);
           }
-          __syncwarp();
+          tc_commit(&bars->s_full[sb]);  // also frees the K slot
+          if (j == I.n_kv - 1) tc_commit(&bars->q_empty[qb]);
         }
-        if (j > 0) {
-          const uint32_t pt = s_ctr - 1;  // running index of tile j - 1
-          ok = warp_mbar_wait(&bars->p_full[prev_sb], (pt / kSB) & 1u, abort, p.status) &&
-               warp_mbar_wait(&bars->v_full[prev_slot], prev_par, abort, p.status);
-          if (!ok) break;
-          // keys past kv_len in the request's last tile: zero their V rows so that
-          // stale values cannot reach O through a zero weight
-          const int valid = I.kv - (j - 1) * kBN;
-          if (valid < kBN) {
-            const uint32_t vt = smem_u32(sV + prev_slot * kTileBytes);
-            for (int i = lane; i < (kBN - valid) * 16; i += 32) {
-              const int rr = valid + i / 16, c16 = i % 16;
-              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vt + (c16 / 8) * kHalf + rr * 128 +
-                                                                          (c16 % 8) * 16),
-                           "r"(0)
-                           : "memory");
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t va = sVa + prev_slot * kTileBytes;
-            const uint32_t pa = tmem + col_s(prev_sb);  // P: 64 columns of bf16 pairs
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              tc_mma_f16_tmem_a(tmem + kColO, pa + 8 * kk, sw128_desc(va + kk * 2048, kHalf, 1024), idesc_pv,
-                                (j > 1 || kk > 0) ? 1u : 0u);
-            tc_commit(&bars->pv_done[prev_sb]);
-            tc_commit(&bars->v_empty[prev_slot]);
-            tc_commit(&bars->s_empty[prev_sb]);
-          }
-          __syncwarp();
-          ++pv_ctr;
-        }
-        if (j < I.n_kv) {
-          prev_slot = slot;
-          prev_par = par;
-          prev_sb = sb;
-          ++kv_ctr;
-          ++s_ctr;
-        }
+        __syncwarp();
       }
-      if (ok && I.n_kv == 0 && lane == 0) tc_commit(&bars->q_empty[qb]);
+      if (!ok) break;
+      if (I.n_kv == 0 && lane == 0) mbar_arrive(&bars->q_empty[qb]);
       __syncwarp();
     }
     // all MMAs of this thread complete before TMEM is released
+    if (lane == 0) {
+      tc_commit(&bars->drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&bars->drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpPV) {
+    // ---------------------------------------------------------- O += P V
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, 1);
+    const uint32_t sVa = smem_u32(sV);
+    uint32_t kv_ctr = 0;
+    bool ok = true;
+    PItem nxt = prefill_item_or_empty(p, blockIdx.x, n_items);
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const PItem I = nxt;
+      nxt = prefill_item_or_empty(p, it + gridDim.x, n_items);
+      for (int j = 0; j < I.n_kv; ++j, ++kv_ctr) {
+        const int slot = kv_ctr % kVSlots;
+        const int sb = kv_ctr % kSB;
+        ok = warp_mbar_wait(&bars->p_full[sb], (kv_ctr / kSB) & 1u, abort, p.status) &&
+             warp_mbar_wait(&bars->v_full[slot], (kv_ctr / kVSlots) & 1u, abort, p.status);
+        if (!ok) break;
+        // keys past kv_len in the request's last tile: zero their V rows so that
+        // stale values cannot reach O through a zero weight
+        const int valid = I.kv - j * kBN;
+        if (valid < kBN) {
+          const uint32_t vt = sVa + slot * kTileBytes;
+          for (int i = lane; i < (kBN - valid) * 16; i += 32) {
+            const int rr = valid + i / 16, c16 = i % 16;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vt + (c16 / 8) * kHalf + rr * 128 +
+                                                                        (c16 % 8) * 16),
+                         "r"(0)
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint64_t dv = sw128_desc(sVa + slot * kTileBytes, kHalf, 1024);
+          const uint32_t pa = tmem + col_s(sb);  // P: 64 columns of bf16 pairs
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            tc_mma_f16_tmem_a(tmem + kColO, pa + 8 * kk, desc_advance(dv, kk * 2048), idesc_pv,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&bars->pv_done[sb]);  // also frees the V slot and the S buffer
+        }
+        __syncwarp();
+      }
+    }
     if (lane == 0) {
       tc_commit(&bars->drain);
       const uint64_t t0 = globaltimer_ns();
@@ -360,15 +436,29 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-    uint32_t s_ctr = 0, o_phase = 0;
+    uint32_t s_ctr = 0, o_phase = 0, it_ctr = 0;
     const bool o_issuer = (warp == 2 && lane == 0);
+    int pending_q = -1;  // Q buffer holding an O tile whose TMA store may still read it
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const PItem I = prefill_item(p, it);
+    PItem nxt = prefill_item_or_empty(p, blockIdx.x, n_items);
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++it_ctr) {
+      const PItem I = nxt;
+      nxt = prefill_item_or_empty(p, it + gridDim.x, n_items);
+      const int qb = it_ctr & 1;
+      // Once the previous item's staged O tile has been read by its TMA store,
+      // its Q buffer may be reloaded. Waited for after this item's first tile
+      // (or at its epilogue), when the store has long finished.
+      auto release_staged = [&]() {
+        if (o_issuer && pending_q >= 0) {
+          bulk_wait_read_all();
+          mbar_arrive(&bars->q_empty[pending_q]);
+          pending_q = -1;
+        }
+      };
       const int lim = I.kv - I.qo_len + I.qt * kBM + row;  // last key this row may see (causal)
-      // l: sum of the bf16-rounded weights that enter P V (normalises O so its
-      // weights sum to one); l_exact: sum of the unrounded weights (for the lse)
-      float m = -INFINITY, l = 0.f, l_exact = 0.f;
+      // l: sum of the weights (normalises O, gives the lse); P enters P V
+      // rounded to bf16, an unbiased rounding far inside the output tolerance
+      float m = -INFINITY, l = 0.f;
       for (int j = 0; j < I.n_kv; ++j) {
         const int sb = s_ctr % kSB;
         ok = warp_mbar_wait(&bars->s_full[sb], (s_ctr / kSB) & 1u, abort, p.status);
@@ -391,13 +481,13 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (full_tile) {
 #pragma unroll
-          for (int e = 0; e < kBN; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(v[e]));
+          for (int e = 0; e < kBN; e += 2)
+            mx[(e / 2) & 3] = fmax3(mx[(e / 2) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
         } else {
 #pragma unroll
-          for (int e = 0; e < kBN; ++e) {
-            const float x = __uint_as_float(v[e]);
-            mx[e & 3] = fmaxf(mx[e & 3], e < ncol ? x : -INFINITY);
-          }
+          for (int e = 0; e < kBN; e += 2)
+            mx[(e / 2) & 3] = fmax3(mx[(e / 2) & 3], e < ncol ? __uint_as_float(v[e]) : -INFINITY,
+                                    e + 1 < ncol ? __uint_as_float(v[e + 1]) : -INFINITY);
         }
         const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         float m_new = m;
@@ -423,7 +513,6 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
           tc_fence_after();
           const float alpha = rescale ? exp2f(m - m_new) : 1.0f;
           l *= alpha;
-          l_exact *= alpha;
 #pragma unroll
           for (int c = 0; c < kD / 32; ++c) {
             uint32_t o[32];
@@ -440,7 +529,6 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         // columns get the argument -inf (weight 0). Sums in packed pairs.
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m, -m);
         float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        float2 le2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         uint32_t w[kBN / 2];
 #pragma unroll
         for (int e = 0; e < kBN; e += 2) {
@@ -450,13 +538,10 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
             x.y = e + 1 < ncol ? x.y : -INFINITY;
           }
           const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          const uint32_t pk = pack_bf16x2(pe.x, pe.y);
-          w[e / 2] = pk;
-          ls2[(e / 2) & 1] = fadd2(ls2[(e / 2) & 1], make_float2(bf16_lo(pk), bf16_hi(pk)));
-          le2[(e / 2) & 1] = fadd2(le2[(e / 2) & 1], pe);
+          w[e / 2] = pack_bf16x2(pe.x, pe.y);
+          ls2[(e / 2) & 1] = fadd2(ls2[(e / 2) & 1], pe);
         }
         l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
-        l_exact += (le2[0].x + le2[0].y) + (le2[1].x + le2[1].y);
         tmem_st32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(w + 0));
         tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(w + 32));
         tmem_wait_st();
@@ -464,8 +549,10 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full[sb]);
         ++s_ctr;
+        if (j == 0) release_staged();
       }
       if (!ok) break;
+      release_staged();
       // ---- epilogue: O / l and the log-sum-exp, once the last P V is done
       if (I.n_kv > 0) {
         const uint32_t last = s_ctr - 1;
@@ -487,16 +574,12 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
 #pragma unroll
         for (int e = 0; e < kD; ++e) v[e] = 0u;
       }
-      if (p.o_dtype == PD_BF16 && I.rows == kBM) {
-        // full tile: stage bf16 O (128-byte swizzled like Q) and write it with
-        // two TMA stores; the staging buffer is reused once the previous
-        // stores have read it
-        if (o_issuer) bulk_wait_read_all();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->o_sync);
-        ok = warp_mbar_wait(&bars->o_sync, o_phase & 1u, abort, p.status);
-        ++o_phase;
-        if (!ok) break;
+      const bool staged = p.o_dtype == PD_BF16 && I.rows == kBM;
+      if (staged) {
+        // full tile: stage bf16 O (128-byte swizzled like Q) in the item's Q
+        // buffer, free now that its last S product has completed, and write it
+        // with two TMA stores
+        uint8_t* sO = sQ + qb * kTileBytes;
         const uint32_t so = smem_u32(sO);
 #pragma unroll
         for (int k = 0; k < kD / 8; ++k) {
@@ -518,6 +601,7 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
           tma_store_3d(&tm_o, 0, I.h, I.q0, sO);
           tma_store_3d(&tm_o, 64, I.h, I.q0, sO + kHalf);
           bulk_commit_group();
+          pending_q = qb;
         }
       } else if (store) {
         if (p.o_dtype == PD_BF16) {
@@ -541,7 +625,8 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       }
       if (store && p.lse != nullptr)
         p.lse[(int64_t)(I.q0 + row) * p.hq + I.h] =
-            (I.n_kv > 0 && l_exact > 0.f) ? (m + log2f(l_exact)) * kLn2 : -INFINITY;
+            (I.n_kv > 0 && l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+      if (o_issuer && !staged) mbar_arrive(&bars->q_empty[qb]);  // nothing staged in this Q buffer
       tc_fence_before();
     }
     if (o_issuer) bulk_wait_all();
@@ -558,6 +643,416 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------ paired kernel
+// Two adjacent 128-row q tiles (A and B) of one (request, query head) per
+// item. Each tile is its own pipeline: an MMA warp, 256 TMEM columns (S/P at
+// +0, O at +128) and a softmax warpgroup, so that while one warpgroup waits on
+// tensor memory or the tensor core the other computes. K and V tiles are
+// loaded once for both. Warps: 0 Q and K loads, 1 V loads, 2 / 3 MMA of A / B,
+// 4-7 softmax of A, 8-11 softmax of B. The load and MMA warpgroup gives
+// registers to the two softmax warpgroups.
+constexpr int kThreadsP2 = 384;
+constexpr uint32_t kP2OffQ = 0;               // Q_A, Q_B
+constexpr uint32_t kP2OffK = 2 * kTileBytes;  // 2 slots
+constexpr uint32_t kP2OffV = 4 * kTileBytes;  // 2 slots
+constexpr uint32_t kP2OffBar = 6 * kTileBytes;
+constexpr size_t kP2Smem = 6 * kTileBytes + 256 + 1024;
+constexpr uint32_t kP2RegsLaunch = 168;  // 65536 / 384, rounded down to a multiple of 8
+constexpr uint32_t kP2RegsLow = 56, kP2RegsHigh = 216;
+static_assert(128 * kP2RegsLow + 256 * kP2RegsHigh <= kThreadsP2 * kP2RegsLaunch,
+              "register split within what the block is launched with");
+
+struct Bars2 {
+  uint64_t q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t s_full[2], p_full[2], pv_done[2], drain[2];
+  uint32_t tmem_slot;
+  int abort;
+};
+static_assert(sizeof(Bars2) <= 256, "barrier block");
+
+struct PItem2 {
+  int r, h, g, q0, qt0, qo_len, kv, n, pbase, need;
+  int rows0, rows1, nkv0, nkv1;
+};
+
+__device__ __forceinline__ PItem2 prefill_item2(const PrefillParams& p, int it) {
+  PItem2 I;
+  const int rq = it / p.hq;
+  I.h = it - rq * p.hq;
+  const int2 v = p.rq_list[rq];
+  I.r = v.x;
+  I.qt0 = 2 * v.y;
+  I.g = I.h / p.group;
+  const int a = p.qo_indptr[I.r];
+  I.qo_len = p.qo_indptr[I.r + 1] - a;
+  I.q0 = a + I.qt0 * kBM;
+  I.kv = p.kv_len[I.r];
+  const int r0 = I.qo_len - I.qt0 * kBM, r1 = r0 - kBM;
+  I.rows0 = r0 <= 0 ? 0 : min(kBM, r0);
+  I.rows1 = r1 <= 0 ? 0 : min(kBM, r1);
+  I.nkv0 = I.rows0 > 0 ? kv_tiles(I.qt0, I.qo_len, I.kv, p.causal) : 0;
+  I.nkv1 = I.rows1 > 0 ? kv_tiles(I.qt0 + 1, I.qo_len, I.kv, p.causal) : 0;
+  I.n = max(I.nkv0, I.nkv1);
+  I.pbase = p.page_indptr[I.r];
+  I.need = (I.kv + p.page_size - 1) / p.page_size;
+  return I;
+}
+
+__device__ __forceinline__ PItem2 prefill_item2_or_empty(const PrefillParams& p, int it, int n_items) {
+  if (it < n_items) return prefill_item2(p, it);
+  PItem2 I{};
+  return I;
+}
+
+__global__ void __launch_bounds__(kThreadsP2, 1)
+    prefill2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base + kP2OffQ;
+  uint8_t* sK = base + kP2OffK;
+  uint8_t* sV = base + kP2OffV;
+  Bars2* bars = reinterpret_cast<Bars2*>(base + kP2OffBar);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 2);  // one arrival per MMA warp
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 2);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 2);
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], 4);
+      mbar_init(&bars->pv_done[i], 1);
+      mbar_init(&bars->drain[i], 1);
+    }
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+  }
+  if (warp == 2) {
+    tmem_alloc(&bars->tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  pdl_wait_primary();  // the plan kernel's item list
+  const int n_items = p.hdr[0];
+
+  if (warp < 4) {
+    regs_shrink<kP2RegsLow>();  // each register budget dominates its warpgroup's code
+  if (warp < 2) {
+    // ------------------------------------------------------------- producers
+    const bool is_v = warp == 1;
+    uint32_t it_ctr = 0, kv_ctr = 0;
+    PItem2 nxt = prefill_item2_or_empty(p, blockIdx.x, n_items);
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++it_ctr) {
+      const PItem2 I = nxt;
+      nxt = prefill_item2_or_empty(p, it + gridDim.x, n_items);
+      if (!is_v) {
+        if (!warp_mbar_wait(&bars->q_empty, (it_ctr & 1u) ^ 1u, abort, p.status)) break;
+        if (lane == 0) {
+          const bool two = I.rows1 > 0;
+          mbar_arrive_expect_tx(&bars->q_full, kTileBytes * (two ? 2u : 1u));
+          tma_load_3d(sQ, &tm_q, 0, I.h, I.q0, &bars->q_full);
+          tma_load_3d(sQ + kHalf, &tm_q, 64, I.h, I.q0, &bars->q_full);
+          if (two) {
+            tma_load_3d(sQ + kTileBytes, &tm_q, 0, I.h, I.q0 + kBM, &bars->q_full);
+            tma_load_3d(sQ + kTileBytes + kHalf, &tm_q, 64, I.h, I.q0 + kBM, &bars->q_full);
+          }
+        }
+        __syncwarp();
+      }
+      bool ok = true;
+      for (int j = 0; j < I.n && ok; ++j, ++kv_ctr) {
+        const int slot = kv_ctr & 1;
+        const uint32_t par = ((kv_ctr >> 1) & 1u) ^ 1u;
+        const TileBox box = tile_box(p, I.pbase, I.need, j, lane);
+        if (!is_v) {
+          ok = warp_mbar_wait(&bars->k_empty[slot], par, abort, p.status);
+          if (ok) load_kv_tile(p, box, &tm_k, I.g, sK + slot * kTileBytes, &bars->k_full[slot], lane);
+        } else {
+          ok = warp_mbar_wait(&bars->v_empty[slot], par, abort, p.status);
+          if (ok) load_kv_tile(p, box, &tm_v, I.g, sV + slot * kTileBytes, &bars->v_full[slot], lane);
+        }
+      }
+      if (!ok) break;
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------------ MMA
+    // Stream X: S = Q_X K_j^T into its S columns; its softmax warpgroup writes
+    // P over S; O_X += P V_j. One S buffer per stream, so S of the next tile
+    // waits for the previous P V product; the other stream fills the gap.
+    const int X = warp - 2;
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, 1);
+    const uint32_t sKa = smem_u32(sK), sVa = smem_u32(sV);
+    const uint64_t dq = sw128_desc(smem_u32(sQ) + X * kTileBytes, 16, 1024);
+    const uint32_t tS = tmem + X * 256, tO = tS + 128;
+    uint32_t it_ctr = 0, kv_ctr = 0, t_ctr = 0;
+    bool ok = true;
+    PItem2 nxt = prefill_item2_or_empty(p, blockIdx.x, n_items);
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++it_ctr) {
+      const PItem2 I = nxt;
+      nxt = prefill_item2_or_empty(p, it + gridDim.x, n_items);
+      const int nX = X ? I.nkv1 : I.nkv0;
+      ok = warp_mbar_wait(&bars->q_full, it_ctr & 1u, abort, p.status);
+      if (!ok) break;
+      tc_fence_after();
+      int t_item = 0;
+      for (int j = 0; j < I.n; ++j, ++kv_ctr) {
+        const int slot = kv_ctr & 1;
+        const uint32_t par = (kv_ctr >> 1) & 1u;
+        ok = warp_mbar_wait(&bars->k_full[slot], par, abort, p.status);
+        if (!ok) break;
+        if (j < nX) {
+          // the S columns hold P of the previous tile until its P V completes
+          if (t_ctr > 0) {
+            ok = warp_mbar_wait(&bars->pv_done[X], (t_ctr - 1) & 1u, abort, p.status);
+            if (!ok) break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint64_t dk = sw128_desc(sKa + slot * kTileBytes, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t off = (kk / 4) * kHalf + (kk % 4) * 32;
+              tc_mma_f16(tS, desc_advance(dq, off), desc_advance(dk, off), idesc_s, kk > 0);
+            }
+            tc_commit(&bars->s_full[X]);
+            tc_commit(&bars->k_empty[slot]);
+            if (j == nX - 1) tc_commit(&bars->q_empty);
+          }
+          __syncwarp();
+          ok = warp_mbar_wait(&bars->p_full[X], t_ctr & 1u, abort, p.status) &&
+               warp_mbar_wait(&bars->v_full[slot], par, abort, p.status);
+          if (!ok) break;
+          // keys past kv_len in the request's last tile: zero their V rows so that
+          // stale values cannot reach O through a zero weight (both streams may
+          // write the same zeros)
+          const int valid = I.kv - j * kBN;
+          if (valid < kBN) {
+            const uint32_t vt = sVa + slot * kTileBytes;
+            for (int i = lane; i < (kBN - valid) * 16; i += 32) {
+              const int rr = valid + i / 16, c16 = i % 16;
+              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vt + (c16 / 8) * kHalf + rr * 128 +
+                                                                          (c16 % 8) * 16),
+                           "r"(0)
+                           : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint64_t dv = sw128_desc(sVa + slot * kTileBytes, kHalf, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              tc_mma_f16_tmem_a(tO, tS + 8 * kk, desc_advance(dv, kk * 2048), idesc_pv,
+                                (t_item > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(&bars->pv_done[X]);
+            tc_commit(&bars->v_empty[slot]);
+          }
+          __syncwarp();
+          ++t_ctr;
+          ++t_item;
+        } else {
+          // a tile only the other stream uses: give back this stream's share
+          if (lane == 0) mbar_arrive(&bars->k_empty[slot]);
+          ok = warp_mbar_wait(&bars->v_full[slot], par, abort, p.status);
+          if (!ok) break;
+          if (lane == 0) mbar_arrive(&bars->v_empty[slot]);
+          __syncwarp();
+        }
+      }
+      if (!ok) break;
+      if (nX == 0 && lane == 0) mbar_arrive(&bars->q_empty);
+      __syncwarp();
+    }
+    // all MMAs of this thread complete before TMEM is released
+    if (lane == 0) {
+      tc_commit(&bars->drain[X]);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&bars->drain[X], 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+    __syncwarp();
+  }
+  } else {
+    regs_grow<kP2RegsHigh>();
+    // --------------------------------------------------- softmax / epilogue
+    const int X = warp >= 8 ? 1 : 0;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16) + X * 256;  // S at +0, O at +128
+    uint32_t t_ctr = 0;
+    bool ok = true;
+    PItem2 nxt = prefill_item2_or_empty(p, blockIdx.x, n_items);
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const PItem2 I = nxt;
+      nxt = prefill_item2_or_empty(p, it + gridDim.x, n_items);
+      const int nX = X ? I.nkv1 : I.nkv0;
+      const int rowsX = X ? I.rows1 : I.rows0;
+      if (rowsX == 0) continue;
+      const int q0 = I.q0 + X * kBM;
+      const int lim = I.kv - I.qo_len + (I.qt0 + X) * kBM + row;  // last key this row may see (causal)
+      // l: sum of the bf16-rounded weights that enter P V (normalises O so its
+      // weights sum to one); l_exact: sum of the unrounded weights (for the lse)
+      float m = -INFINITY, l = 0.f, l_exact = 0.f;
+      for (int j = 0; j < nX; ++j) {
+        ok = warp_mbar_wait(&bars->s_full[X], t_ctr & 1u, abort, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        const int k0 = j * kBN;
+        int ncol = min(kBN, I.kv - k0);
+        if (p.causal) ncol = min(ncol, lim - k0 + 1);
+        uint32_t v[kBN];
+        tmem_ld32(t_lane + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
+        tmem_ld32(t_lane + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld32(t_lane + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
+        tmem_ld32(t_lane + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+        tmem_wait_ld();
+        const bool full_tile = __all_sync(0xffffffffu, ncol >= kBN);
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (full_tile) {
+#pragma unroll
+          for (int e = 0; e < kBN; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(v[e]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < kBN; ++e) {
+            const float x = __uint_as_float(v[e]);
+            mx[e & 3] = fmaxf(mx[e & 3], e < ncol ? x : -INFINITY);
+          }
+        }
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        float m_new = m;
+        bool rescale = false;
+        if (mt > -INFINITY) {
+          const float ms = mt * p.scale_log2;
+          if (m == -INFINITY) {
+            m_new = ms;
+          } else if (ms > m + kRescaleThreshold) {
+            m_new = ms;
+            rescale = true;
+          }
+        }
+        // warp-uniform rescale of this warp's O rows after the previous P V
+        if (__any_sync(0xffffffffu, rescale)) {
+          ok = warp_mbar_wait(&bars->pv_done[X], (t_ctr - 1) & 1u, abort, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          const float alpha = rescale ? exp2f(m - m_new) : 1.0f;
+          l *= alpha;
+          l_exact *= alpha;
+#pragma unroll
+          for (int c = 0; c < kD / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(t_lane + 128 + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(t_lane + 128 + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+        m = m_new;
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m, -m);
+        float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        float2 le2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        uint32_t w[kBN / 2];
+#pragma unroll
+        for (int e = 0; e < kBN; e += 2) {
+          float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nm2);
+          if (!full_tile) {
+            x.x = e < ncol ? x.x : -INFINITY;
+            x.y = e + 1 < ncol ? x.y : -INFINITY;
+          }
+          const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          const uint32_t pk = pack_bf16x2(pe.x, pe.y);
+          w[e / 2] = pk;
+          ls2[(e / 2) & 1] = fadd2(ls2[(e / 2) & 1], make_float2(bf16_lo(pk), bf16_hi(pk)));
+          le2[(e / 2) & 1] = fadd2(le2[(e / 2) & 1], pe);
+        }
+        l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
+        l_exact += (le2[0].x + le2[0].y) + (le2[1].x + le2[1].y);
+        tmem_st32(t_lane + 0, *reinterpret_cast<uint32_t(*)[32]>(w + 0));
+        tmem_st32(t_lane + 32, *reinterpret_cast<uint32_t(*)[32]>(w + 32));
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full[X]);
+        ++t_ctr;
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l and the log-sum-exp, once the last P V is done
+      if (nX > 0) {
+        ok = warp_mbar_wait(&bars->pv_done[X], (t_ctr - 1) & 1u, abort, p.status);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+      const bool store = row < rowsX;
+      const int64_t orow = ((int64_t)(q0 + row) * p.hq + I.h) * kD;
+      uint32_t v[kD];
+      if (nX > 0) {
+        tmem_ld32(t_lane + 128, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
+        tmem_ld32(t_lane + 160, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld32(t_lane + 192, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
+        tmem_ld32(t_lane + 224, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < kD; ++e) v[e] = 0u;
+      }
+      if (store) {
+        if (p.o_dtype == PD_BF16) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow);
+#pragma unroll
+          for (int k = 0; k < kD / 8; ++k) {
+            uint4 u;
+            u.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l);
+            u.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l);
+            u.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l);
+            u.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l);
+            dst[k] = u;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow);
+#pragma unroll
+          for (int k = 0; k < kD / 4; ++k)
+            dst[k] = make_float4(__uint_as_float(v[4 * k]) * inv_l, __uint_as_float(v[4 * k + 1]) * inv_l,
+                                 __uint_as_float(v[4 * k + 2]) * inv_l, __uint_as_float(v[4 * k + 3]) * inv_l);
+        }
+        if (p.lse != nullptr)
+          p.lse[(int64_t)(q0 + row) * p.hq + I.h] =
+              (nX > 0 && l_exact > 0.f) ? (m + log2f(l_exact)) * kLn2 : -INFINITY;
+      }
+      tc_fence_before();
+    }
+  }
+
+  // Normally every copy has been consumed here. After an abort, copies may still
+  // be in flight: give them a bounded 2 ms to land before shared memory is freed.
+  if (*abort && warp == 0 && lane == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 2000000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------- host
@@ -583,11 +1078,18 @@ int prefill_supported(int32_t kv_dtype, int32_t head_dim, int32_t page_size) {
   return PD_OK;
 }
 
+// 1: items of two q tiles on the two-pipeline kernel; 0: one q tile per item.
+#ifndef PD_PREFILL_PAIR
+#define PD_PREFILL_PAIR 0
+#endif
+
 int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const void* v_pool, cudaStream_t stream) {
+  p.pair = PD_PREFILL_PAIR;
   CUtensorMap tq, tk, tv, to;
   const int pb = p.page_size < kBN ? p.page_size : kBN;
   memset(&to, 0, sizeof(to));
-  if (p.o_dtype == PD_BF16 && !make_rows_map(&to, p.o, PD_BF16, p.total_qo, p.hq, kD, 64, kBM, true)) return PD_ERR_CUDA;
+  if (!p.pair && p.o_dtype == PD_BF16 && !make_rows_map(&to, p.o, PD_BF16, p.total_qo, p.hq, kD, 64, kBM, true))
+    return PD_ERR_CUDA;
   if (!make_rows_map(&tq, q, PD_BF16, p.total_qo, p.hq, kD, 64, kBM, true) ||
       !make_pool_map(&tk, k_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true) ||
       !make_pool_map(&tv, v_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true))
@@ -597,19 +1099,34 @@ int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const vo
   if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;
   if (configured_device != dev) {
     if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrefillSmem) !=
-        cudaSuccess)
+            cudaSuccess ||
+        cudaFuncSetAttribute(prefill2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP2Smem) !=
+            cudaSuccess)
       return PD_ERR_CUDA;
     configured_device = dev;
   }
   prefill_plan_kernel<<<1, 1024, 0, stream>>>(p);
   int64_t grid = device_sm_count();
-  const int64_t max_items = (int64_t)p.max_rq * p.hq;
+  const int64_t max_items = (int64_t)(p.pair ? (p.max_rq + 1) / 2 + p.batch : p.max_rq) * p.hq;
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
+  // A programmatic dependent of the plan (CTAs set up while it finishes),
+  // except when timed alone through the profiling events.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(p.pair ? kThreadsP2 : kThreadsPf);
+  cfg.dynamicSmemBytes = p.pair ? kP2Smem : kPrefillSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = profile_events().start != nullptr ? 0 : 1;
   profile_begin(stream);
-  prefill_kernel<<<(unsigned)grid, kThreadsPf, kPrefillSmem, stream>>>(tq, tk, tv, to, p);
+  const cudaError_t e = p.pair ? cudaLaunchKernelEx(&cfg, prefill2_kernel, tq, tk, tv, p)
+                               : cudaLaunchKernelEx(&cfg, prefill_kernel, tq, tk, tv, to, p);
   profile_end(stream);
-  return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
 }
 
 }  // namespace pd

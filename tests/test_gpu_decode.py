@@ -114,3 +114,17 @@ def test_decode_is_deterministic():
     a, la = run_decode(case)
     b, lb = run_decode(case)
     assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+def test_decode_many_requests_with_empty_ones():
+    # more requests than the planner's block of threads; every 97th request has
+    # no cached key (o = 0, lse = -inf) and the rest mix one- and many-chunk splits
+    rng = np.random.default_rng(107)
+    kv = rng.integers(1, 700, size=1300)
+    kv[::97] = 0
+    case = wl.make_attn_case(107, [1] * 1300, kv, 4, 2, 64, 16, wl.F32, causal=False)
+    o, lse = run_decode(case)
+    empty = torch.from_numpy(kv == 0).cuda()
+    assert torch.all(o[empty] == 0) and torch.all(torch.isneginf(lse[empty]))
+    o_ref, lse_ref = oracle.attention_case(case)
+    compare(o, lse, o_ref, lse_ref, case.dtype)
