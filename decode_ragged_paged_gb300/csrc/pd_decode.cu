@@ -56,7 +56,10 @@ constexpr int kNC = PD_DECODE_WARPS;          // consumer warps
 constexpr int kPL = PD_DECODE_PRODUCER_LANES;  // issuing lanes of the producer warp
 constexpr int kThreads = (kNC + 1) * 32;
 static_assert(kPL >= 1 && kPL <= 32, "producer lanes");
-constexpr int kMaxChunk = 512;                // longest chunk (tokens) a work item covers
+#ifndef PD_DECODE_MAX_CHUNK
+#define PD_DECODE_MAX_CHUNK 512
+#endif
+constexpr int kMaxChunk = PD_DECODE_MAX_CHUNK;  // longest chunk (tokens) a work item covers
 constexpr int kRingBytes = PD_DECODE_RING_KB * 1024;
 static_assert(kTS % 4 == 0 && kMaxChunk % kTS == 0, "stage size");
 constexpr unsigned kFull = 0xffffffffu;
@@ -69,7 +72,10 @@ struct Geo {
   static constexpr int kEpv = 16 / ES;                // elements per vector
   static constexpr int kE = kVecPerLane * kEpv;       // elements per lane = D / 8
   static constexpr int kStageBytes = kTS * kRowBytes;
-  static constexpr int kStages = kRingBytes / kStageBytes < 32 ? kRingBytes / kStageBytes : 32;
+  // as many stages as the ring holds (at most 32), rounded down to a multiple of
+  // the consumer warps
+  static constexpr int kStagesRaw = kRingBytes / kStageBytes < 32 ? kRingBytes / kStageBytes : 32;
+  static constexpr int kStages = kStagesRaw / kNC * kNC;
   static_assert(kVecPerLane >= 1, "row too short");
   // Within a K or V phase stage s belongs to consumer warp s % kNC and uses ring
   // slot (running index) % kStages. With kStages a multiple of kNC every use of

@@ -62,11 +62,10 @@ int launch_decode(DecodeParams& p, int32_t kv_dtype, cudaStream_t stream);
 // ----------------------------------------------------------------- prefill
 // Workspace of the tensor-core prefill (offsets 256-byte aligned):
 //   hdr      int32[64]     hdr[0] = work items (q tiles x query heads)
-//   rq_list  int2[max_rq]  (request, q tile or pair of q tiles) ordered by decreasing KV-tile count
+//   rq_list  int2[max_rq]  (request, q tile) ordered by decreasing KV-tile count
 struct PrefillParams {
   int32_t batch, hq, hkv, group, page_size, num_pages, total_qo, max_qo_len, max_kv_len, causal, o_dtype;
   int32_t max_rq;
-  int32_t pair;      // items cover two adjacent 128-row q tiles (set by launch_prefill)
   float scale_log2;  // softmax scale times log2(e)
   const int32_t* qo_indptr;
   const int32_t* kv_len;

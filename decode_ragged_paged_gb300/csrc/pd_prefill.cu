@@ -15,14 +15,17 @@
 //             and arrive as zeros;
 //   warp 6    TMA producer of V tiles (2-slot ring), same boxes;
 //   warp 1    allocates 512 TMEM columns and issues S = Q K^T (tcgen05.mma)
-//             into one of three S buffers;
-//   warp 7    issues O += P V into the O buffer with P read from tensor
-//             memory (two issuing warps: one thread's tcgen05.mma issue rate
-//             and commits limited a single issuer);
+//             into one of two S buffers;
+//   warp 7    issues O += P V into the item's O buffer (two, alternating
+//             between items) with P read from tensor memory (two issuing
+//             warps: one thread's tcgen05.mma issue rate and commits limited a
+//             single issuer);
 //   warps 2-5 one query row per thread: one-pass online softmax on S read from
 //             TMEM, P written back over S as bf16 pairs, O rescaled in TMEM
-//             only when the running max grows by more than 2^8, final O / l
-//             staged in shared memory and stored by TMA, log-sum-exp written.
+//             only when the running max grows by more than 2^8; an item's
+//             epilogue (O / l, log-sum-exp) runs after the next item's first
+//             tile, a full bf16 O tile staged in the item's Q buffer and
+//             stored by TMA.
 // Every wait is bounded; on a timeout the CTA records PD_DEV_TIMEOUT, drains
 // and frees its TMEM.
 #include <math.h>
@@ -45,9 +48,11 @@ constexpr int kWarpPV = 7;        // the warp that issues O += P V
 constexpr uint32_t kTileBytes = kBM * kD * 2;  // one bf16 128 x 128 tile
 constexpr uint32_t kHalf = kTileBytes / 2;     // one 64-column half: 128 rows x 128 B
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSB = 3;                         // S / P buffers in TMEM (128 columns each)
-constexpr uint32_t kColO = kSB * 128;          // O accumulator after them
+constexpr int kSB = 2;                         // S / P buffers in TMEM (128 columns each)
+// two O accumulators after them, alternating between consecutive items
 __device__ __forceinline__ uint32_t col_s(int b) { return (uint32_t)b * 128; }
+__device__ __forceinline__ uint32_t col_o(int b) { return (uint32_t)(kSB + b) * 128; }
+static_assert((kSB + 2) * 128 <= 512, "TMEM columns");
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 constexpr int kBuckets = 1024;
 
@@ -64,13 +69,17 @@ constexpr uint32_t kOffQ = 0;                  // 2 tiles
 constexpr int kKSlots = PD_PREFILL_K_SLOTS;
 constexpr int kVSlots = PD_PREFILL_V_SLOTS;
 static_assert(kKSlots >= 2 && kVSlots >= 2 && kKSlots + kVSlots <= 5, "ring depths");
+// A V slot is freed by the pv_done phase of its previous tile. A waiter on that
+// barrier must never fall two phases behind, which holds while the ring is no
+// deeper than the S buffers (K slots have their own k_empty barriers).
+static_assert(kVSlots <= kSB, "V ring deeper than the S buffers");
 constexpr uint32_t kOffK = 2 * kTileBytes;
 constexpr uint32_t kOffV = (2 + kKSlots) * kTileBytes;
 constexpr uint32_t kOffBar = 7 * kTileBytes;
 constexpr size_t kPrefillSmem = 7 * kTileBytes + 256 + 1024;
 
 struct Bars {
-  uint64_t q_full[2], q_empty[2], k_full[kKSlots], v_full[kVSlots];
+  uint64_t q_full[2], q_empty[2], k_full[kKSlots], k_empty[kKSlots], v_full[kVSlots];
   uint64_t s_full[kSB], p_full[kSB], pv_done[kSB], drain, o_sync;
   uint32_t tmem_slot;
   int abort;
@@ -185,17 +194,10 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
   const int tid = threadIdx.x;
   for (int b = tid; b < kBuckets; b += blockDim.x) hist[b] = 0;
   __syncthreads();
-  // an entry covers one q tile, or two adjacent ones in pair mode (weighed by
-  // the KV tiles of its last tile, the heaviest of the two)
-  const int span = p.pair ? 2 : 1;
   for (int r = tid; r < p.batch; r += blockDim.x) {
     if (!request_ok(p, r)) continue;
     const int qo = p.qo_indptr[r + 1] - p.qo_indptr[r], n = p.kv_len[r];
-    const int tiles = (qo + kBM - 1) / kBM;
-    for (int e = 0; e * span < tiles; ++e) {
-      const int last = min(e * span + span, tiles) - 1;
-      atomicAdd(&hist[min(kv_tiles(last, qo, n, p.causal), kBuckets - 1)], 1);
-    }
+    for (int qt = 0; qt * kBM < qo; ++qt) atomicAdd(&hist[min(kv_tiles(qt, qo, n, p.causal), kBuckets - 1)], 1);
   }
   __syncthreads();
   {
@@ -229,11 +231,9 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
   for (int r = tid; r < p.batch; r += blockDim.x) {
     if (!request_ok(p, r)) continue;
     const int qo = p.qo_indptr[r + 1] - p.qo_indptr[r], n = p.kv_len[r];
-    const int tiles = (qo + kBM - 1) / kBM;
-    for (int e = 0; e * span < tiles; ++e) {
-      const int last = min(e * span + span, tiles) - 1;
-      const int pos = atomicAdd(&cursor[min(kv_tiles(last, qo, n, p.causal), kBuckets - 1)], 1);
-      if (pos < p.max_rq) p.rq_list[pos] = make_int2(r, e);
+    for (int qt = 0; qt * kBM < qo; ++qt) {
+      const int pos = atomicAdd(&cursor[min(kv_tiles(qt, qo, n, p.causal), kBuckets - 1)], 1);
+      if (pos < p.max_rq) p.rq_list[pos] = make_int2(r, qt);
     }
   }
 }
@@ -258,7 +258,10 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       // the item's last S product, and the read of the O tile staged in it
       mbar_init(&bars->q_empty[i], 2);
     }
-    for (int i = 0; i < kKSlots; ++i) mbar_init(&bars->k_full[i], 1);
+    for (int i = 0; i < kKSlots; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+    }
     for (int i = 0; i < kVSlots; ++i) mbar_init(&bars->v_full[i], 1);
     for (int i = 0; i < kSB; ++i) {
       mbar_init(&bars->s_full[i], 1);
@@ -312,13 +315,14 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       for (int j = 0; j < I.n_kv && ok; ++j, ++kv_ctr) {
         const int slot = kv_ctr % depth;
         const TileBox box = tile_box(p, I.pbase, I.need, j, lane);  // page ids read before the slot wait
-        // The slot's previous tile u = kv_ctr - depth is done with it once S_u
-        // (for K) or P_u V_u (for V) has completed; every tile's phase is waited
-        // in order, so a parity wait is never more than one phase behind.
-        if (kv_ctr >= depth) {
+        // A K slot is free again once the S product of its previous tile has
+        // completed (k_empty); a V slot once the P V product of its previous
+        // tile u = kv_ctr - depth has (pv_done, waited for every tile in order).
+        if (!is_v) {
+          ok = warp_mbar_wait(&bars->k_empty[slot], ((kv_ctr / kKSlots) & 1u) ^ 1u, abort, p.status);
+        } else if (kv_ctr >= depth) {
           const uint32_t u = kv_ctr - depth;
-          ok = warp_mbar_wait(is_v ? &bars->pv_done[u % kSB] : &bars->s_full[u % kSB], (u / kSB) & 1u, abort,
-                              p.status);
+          ok = warp_mbar_wait(&bars->pv_done[u % kSB], (u / kSB) & 1u, abort, p.status);
         }
         if (ok) {
           if (!is_v)
@@ -363,7 +367,8 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
             const uint32_t off = (kk / 4) * kHalf + (kk % 4) * 32;
             tc_mma_f16(tmem + col_s(sb), desc_advance(dq, off), desc_advance(dk, off), idesc_s, kk > 0);
           }
-          tc_commit(&bars->s_full[sb]);  // also frees the K slot
+          tc_commit(&bars->s_full[sb]);
+          tc_commit(&bars->k_empty[slot]);
           if (j == I.n_kv - 1) tc_commit(&bars->q_empty[qb]);
         }
         __syncwarp();
@@ -384,12 +389,13 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
     // ---------------------------------------------------------- O += P V
     constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, 1);
     const uint32_t sVa = smem_u32(sV);
-    uint32_t kv_ctr = 0;
+    uint32_t kv_ctr = 0, it_ctr = 0;
     bool ok = true;
     PItem nxt = prefill_item_or_empty(p, blockIdx.x, n_items);
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++it_ctr) {
       const PItem I = nxt;
       nxt = prefill_item_or_empty(p, it + gridDim.x, n_items);
+      const uint32_t t_o = tmem + col_o(it_ctr & 1);  // this item's O accumulator
       for (int j = 0; j < I.n_kv; ++j, ++kv_ctr) {
         const int slot = kv_ctr % kVSlots;
         const int sb = kv_ctr % kSB;
@@ -417,7 +423,7 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
           const uint32_t pa = tmem + col_s(sb);  // P: 64 columns of bf16 pairs
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            tc_mma_f16_tmem_a(tmem + kColO, pa + 8 * kk, desc_advance(dv, kk * 2048), idesc_pv,
+            tc_mma_f16_tmem_a(t_o, pa + 8 * kk, desc_advance(dv, kk * 2048), idesc_pv,
                               (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&bars->pv_done[sb]);  // also frees the V slot and the S buffer
         }
@@ -433,6 +439,9 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
     __syncwarp();
   } else if (warp >= 2 && warp < 6) {
     // --------------------------------------------------- softmax / epilogue
+    // Item i's epilogue is deferred until item i + 1's first tile has been
+    // published: the wait for item i's last P V then overlaps useful work.
+    // Items alternate between the two O accumulators.
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
@@ -440,21 +449,103 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
     const bool o_issuer = (warp == 2 && lane == 0);
     int pending_q = -1;  // Q buffer holding an O tile whose TMA store may still read it
     bool ok = true;
+    struct Pend {
+      int q0, h, rows, n_kv, qb, ob;
+      uint32_t last;  // running index of the item's last tile
+      float m, l;
+    };
+    Pend pend{};
+    bool has_pend = false;
+    // Once a staged O tile has been read by its TMA store, its Q buffer may be
+    // reloaded (the store has long finished when this is called).
+    auto release_staged = [&]() {
+      if (o_issuer && pending_q >= 0) {
+        bulk_wait_read_all();
+        mbar_arrive(&bars->q_empty[pending_q]);
+        pending_q = -1;
+      }
+    };
+    // O / l and the log-sum-exp of a finished item, once its last P V is done.
+    auto epilogue = [&](const Pend& E) -> bool {
+      if (E.n_kv > 0) {
+        if (!warp_mbar_wait(&bars->pv_done[E.last % kSB], (E.last / kSB) & 1u, abort, p.status)) return false;
+        tc_fence_after();
+      }
+      const float inv_l = E.l > 0.f ? 1.0f / E.l : 0.f;
+      const bool store = row < E.rows;
+      const int64_t orow = ((int64_t)(E.q0 + row) * p.hq + E.h) * kD;
+      const uint32_t o_addr = t_lane + col_o(E.ob);
+      uint32_t v[kD];
+      if (E.n_kv > 0) {
+        tmem_ld32(o_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
+        tmem_ld32(o_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld32(o_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
+        tmem_ld32(o_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < kD; ++e) v[e] = 0u;
+      }
+      const bool staged = p.o_dtype == PD_BF16 && E.rows == kBM;
+      if (staged) {
+        // full tile: stage bf16 O (128-byte swizzled like Q) in the item's Q
+        // buffer, free now that its last S product has completed, and write it
+        // with two TMA stores
+        uint8_t* sO = sQ + E.qb * kTileBytes;
+        const uint32_t so = smem_u32(sO);
+#pragma unroll
+        for (int k = 0; k < kD / 8; ++k) {
+          const uint32_t a0 = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l);
+          const uint32_t a1 = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l);
+          const uint32_t a2 = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l);
+          const uint32_t a3 = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l);
+          const uint32_t addr = so + (k / 8) * kHalf + row * 128 + (((k % 8) ^ (row & 7)) * 16);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->o_sync);
+        if (!warp_mbar_wait(&bars->o_sync, o_phase & 1u, abort, p.status)) return false;
+        ++o_phase;
+        if (o_issuer) {
+          tma_store_3d(&tm_o, 0, E.h, E.q0, sO);
+          tma_store_3d(&tm_o, 64, E.h, E.q0, sO + kHalf);
+          bulk_commit_group();
+          pending_q = E.qb;
+        }
+      } else if (store) {
+        if (p.o_dtype == PD_BF16) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow);
+#pragma unroll
+          for (int k = 0; k < kD / 8; ++k) {
+            uint4 u;
+            u.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l);
+            u.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l);
+            u.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l);
+            u.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l);
+            dst[k] = u;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow);
+#pragma unroll
+          for (int k = 0; k < kD / 4; ++k)
+            dst[k] = make_float4(__uint_as_float(v[4 * k]) * inv_l, __uint_as_float(v[4 * k + 1]) * inv_l,
+                                 __uint_as_float(v[4 * k + 2]) * inv_l, __uint_as_float(v[4 * k + 3]) * inv_l);
+        }
+      }
+      if (store && p.lse != nullptr)
+        p.lse[(int64_t)(E.q0 + row) * p.hq + E.h] = (E.n_kv > 0 && E.l > 0.f) ? (E.m + log2f(E.l)) * kLn2 : -INFINITY;
+      if (o_issuer && !staged) mbar_arrive(&bars->q_empty[E.qb]);  // nothing staged in this Q buffer
+      tc_fence_before();
+      return true;
+    };
     PItem nxt = prefill_item_or_empty(p, blockIdx.x, n_items);
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++it_ctr) {
       const PItem I = nxt;
       nxt = prefill_item_or_empty(p, it + gridDim.x, n_items);
-      const int qb = it_ctr & 1;
-      // Once the previous item's staged O tile has been read by its TMA store,
-      // its Q buffer may be reloaded. Waited for after this item's first tile
-      // (or at its epilogue), when the store has long finished.
-      auto release_staged = [&]() {
-        if (o_issuer && pending_q >= 0) {
-          bulk_wait_read_all();
-          mbar_arrive(&bars->q_empty[pending_q]);
-          pending_q = -1;
-        }
-      };
+      const int qb = it_ctr & 1, ob = it_ctr & 1;
+      const uint32_t o_addr = t_lane + col_o(ob);
       const int lim = I.kv - I.qo_len + I.qt * kBM + row;  // last key this row may see (causal)
       // l: sum of the weights (normalises O, gives the lse); P enters P V
       // rounded to bf16, an unbiased rounding far inside the output tolerance
@@ -475,20 +566,18 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
         tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
         tmem_wait_ld();
-        // row max of the tile (four independent chains); columns past ncol are
-        // masked only in tiles where some row of the warp has any
+        // columns past ncol are masked only in tiles where some row of the warp has any
         const bool full_tile = __all_sync(0xffffffffu, ncol >= kBN);
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (full_tile) {
+        if (!full_tile) {
+          // masked keys score -inf: weight 0 below
 #pragma unroll
-          for (int e = 0; e < kBN; e += 2)
-            mx[(e / 2) & 3] = fmax3(mx[(e / 2) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-        } else {
-#pragma unroll
-          for (int e = 0; e < kBN; e += 2)
-            mx[(e / 2) & 3] = fmax3(mx[(e / 2) & 3], e < ncol ? __uint_as_float(v[e]) : -INFINITY,
-                                    e + 1 < ncol ? __uint_as_float(v[e + 1]) : -INFINITY);
+          for (int e = 0; e < kBN; ++e) v[e] = e < ncol ? v[e] : 0xff800000u;
         }
+        // row max of the tile (four independent chains)
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int e = 0; e < kBN; e += 2)
+          mx[(e / 2) & 3] = fmax3(mx[(e / 2) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
         const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         float m_new = m;
         bool rescale = false;
@@ -516,27 +605,23 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
 #pragma unroll
           for (int c = 0; c < kD / 32; ++c) {
             uint32_t o[32];
-            tmem_ld32(t_lane + kColO + c * 32, o);
+            tmem_ld32(o_addr + c * 32, o);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(t_lane + kColO + c * 32, o);
+            tmem_st32(o_addr + c * 32, o);
           }
           tmem_wait_st();
         }
         m = m_new;
-        // P = 2^(s * scale - m) as bf16 pairs, written over the S columns; masked
-        // columns get the argument -inf (weight 0). Sums in packed pairs.
+        // P = 2^(s * scale - m) as bf16 pairs, written over the S columns
+        // (masked columns: -inf, weight 0). Sums in packed pairs.
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m, -m);
         float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         uint32_t w[kBN / 2];
 #pragma unroll
         for (int e = 0; e < kBN; e += 2) {
-          float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nm2);
-          if (!full_tile) {
-            x.x = e < ncol ? x.x : -INFINITY;
-            x.y = e + 1 < ncol ? x.y : -INFINITY;
-          }
+          const float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nm2);
           const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
           w[e / 2] = pack_bf16x2(pe.x, pe.y);
           ls2[(e / 2) & 1] = fadd2(ls2[(e / 2) & 1], pe);
@@ -549,86 +634,34 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full[sb]);
         ++s_ctr;
-        if (j == 0) release_staged();
+        if (j == 0 && has_pend) {
+          // the previous item's epilogue, now that this item's first P is out
+          ok = epilogue(pend);
+          has_pend = false;
+          if (!ok) break;
+        } else {
+          release_staged();
+        }
       }
       if (!ok) break;
       release_staged();
-      // ---- epilogue: O / l and the log-sum-exp, once the last P V is done
-      if (I.n_kv > 0) {
-        const uint32_t last = s_ctr - 1;
-        ok = warp_mbar_wait(&bars->pv_done[last % kSB], (last / kSB) & 1u, abort, p.status);
+      const Pend cur{I.q0, I.h, I.rows, I.n_kv, qb, ob, s_ctr - 1, m, l};
+      if (I.n_kv == 0) {
+        // no tile to overlap with: finish the pending item and this one now
+        if (has_pend) {
+          ok = epilogue(pend);
+          has_pend = false;
+          if (!ok) break;
+          release_staged();
+        }
+        ok = epilogue(cur);
         if (!ok) break;
-        tc_fence_after();
-      }
-      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-      const bool store = row < I.rows;
-      const int64_t orow = ((int64_t)(I.q0 + row) * p.hq + I.h) * kD;
-      uint32_t v[kD];
-      if (I.n_kv > 0) {
-        tmem_ld32(t_lane + kColO + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
-        tmem_ld32(t_lane + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        tmem_ld32(t_lane + kColO + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
-        tmem_ld32(t_lane + kColO + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
-        tmem_wait_ld();
       } else {
-#pragma unroll
-        for (int e = 0; e < kD; ++e) v[e] = 0u;
+        pend = cur;
+        has_pend = true;
       }
-      const bool staged = p.o_dtype == PD_BF16 && I.rows == kBM;
-      if (staged) {
-        // full tile: stage bf16 O (128-byte swizzled like Q) in the item's Q
-        // buffer, free now that its last S product has completed, and write it
-        // with two TMA stores
-        uint8_t* sO = sQ + qb * kTileBytes;
-        const uint32_t so = smem_u32(sO);
-#pragma unroll
-        for (int k = 0; k < kD / 8; ++k) {
-          const uint32_t a0 = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l);
-          const uint32_t a1 = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l);
-          const uint32_t a2 = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l);
-          const uint32_t a3 = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l);
-          const uint32_t addr = so + (k / 8) * kHalf + row * 128 + (((k % 8) ^ (row & 7)) * 16);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a0), "r"(a1), "r"(a2), "r"(a3)
-                       : "memory");
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->o_sync);
-        ok = warp_mbar_wait(&bars->o_sync, o_phase & 1u, abort, p.status);
-        ++o_phase;
-        if (!ok) break;
-        if (o_issuer) {
-          tma_store_3d(&tm_o, 0, I.h, I.q0, sO);
-          tma_store_3d(&tm_o, 64, I.h, I.q0, sO + kHalf);
-          bulk_commit_group();
-          pending_q = qb;
-        }
-      } else if (store) {
-        if (p.o_dtype == PD_BF16) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow);
-#pragma unroll
-          for (int k = 0; k < kD / 8; ++k) {
-            uint4 u;
-            u.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l);
-            u.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l);
-            u.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l);
-            u.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l);
-            dst[k] = u;
-          }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow);
-#pragma unroll
-          for (int k = 0; k < kD / 4; ++k)
-            dst[k] = make_float4(__uint_as_float(v[4 * k]) * inv_l, __uint_as_float(v[4 * k + 1]) * inv_l,
-                                 __uint_as_float(v[4 * k + 2]) * inv_l, __uint_as_float(v[4 * k + 3]) * inv_l);
-        }
-      }
-      if (store && p.lse != nullptr)
-        p.lse[(int64_t)(I.q0 + row) * p.hq + I.h] =
-            (I.n_kv > 0 && l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
-      if (o_issuer && !staged) mbar_arrive(&bars->q_empty[qb]);  // nothing staged in this Q buffer
-      tc_fence_before();
     }
+    if (ok && has_pend) ok = epilogue(pend);
     if (o_issuer) bulk_wait_all();
   }
 
@@ -643,416 +676,6 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-}
-
-// ------------------------------------------------------------ paired kernel
-// Two adjacent 128-row q tiles (A and B) of one (request, query head) per
-// item. Each tile is its own pipeline: an MMA warp, 256 TMEM columns (S/P at
-// +0, O at +128) and a softmax warpgroup, so that while one warpgroup waits on
-// tensor memory or the tensor core the other computes. K and V tiles are
-// loaded once for both. Warps: 0 Q and K loads, 1 V loads, 2 / 3 MMA of A / B,
-// 4-7 softmax of A, 8-11 softmax of B. The load and MMA warpgroup gives
-// registers to the two softmax warpgroups.
-constexpr int kThreadsP2 = 384;
-constexpr uint32_t kP2OffQ = 0;               // Q_A, Q_B
-constexpr uint32_t kP2OffK = 2 * kTileBytes;  // 2 slots
-constexpr uint32_t kP2OffV = 4 * kTileBytes;  // 2 slots
-constexpr uint32_t kP2OffBar = 6 * kTileBytes;
-constexpr size_t kP2Smem = 6 * kTileBytes + 256 + 1024;
-constexpr uint32_t kP2RegsLaunch = 168;  // 65536 / 384, rounded down to a multiple of 8
-constexpr uint32_t kP2RegsLow = 56, kP2RegsHigh = 216;
-static_assert(128 * kP2RegsLow + 256 * kP2RegsHigh <= kThreadsP2 * kP2RegsLaunch,
-              "register split within what the block is launched with");
-
-struct Bars2 {
-  uint64_t q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[2], p_full[2], pv_done[2], drain[2];
-  uint32_t tmem_slot;
-  int abort;
-};
-static_assert(sizeof(Bars2) <= 256, "barrier block");
-
-struct PItem2 {
-  int r, h, g, q0, qt0, qo_len, kv, n, pbase, need;
-  int rows0, rows1, nkv0, nkv1;
-};
-
-__device__ __forceinline__ PItem2 prefill_item2(const PrefillParams& p, int it) {
-  PItem2 I;
-  const int rq = it / p.hq;
-  I.h = it - rq * p.hq;
-  const int2 v = p.rq_list[rq];
-  I.r = v.x;
-  I.qt0 = 2 * v.y;
-  I.g = I.h / p.group;
-  const int a = p.qo_indptr[I.r];
-  I.qo_len = p.qo_indptr[I.r + 1] - a;
-  I.q0 = a + I.qt0 * kBM;
-  I.kv = p.kv_len[I.r];
-  const int r0 = I.qo_len - I.qt0 * kBM, r1 = r0 - kBM;
-  I.rows0 = r0 <= 0 ? 0 : min(kBM, r0);
-  I.rows1 = r1 <= 0 ? 0 : min(kBM, r1);
-  I.nkv0 = I.rows0 > 0 ? kv_tiles(I.qt0, I.qo_len, I.kv, p.causal) : 0;
-  I.nkv1 = I.rows1 > 0 ? kv_tiles(I.qt0 + 1, I.qo_len, I.kv, p.causal) : 0;
-  I.n = max(I.nkv0, I.nkv1);
-  I.pbase = p.page_indptr[I.r];
-  I.need = (I.kv + p.page_size - 1) / p.page_size;
-  return I;
-}
-
-__device__ __forceinline__ PItem2 prefill_item2_or_empty(const PrefillParams& p, int it, int n_items) {
-  if (it < n_items) return prefill_item2(p, it);
-  PItem2 I{};
-  return I;
-}
-
-__global__ void __launch_bounds__(kThreadsP2, 1)
-    prefill2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base + kP2OffQ;
-  uint8_t* sK = base + kP2OffK;
-  uint8_t* sV = base + kP2OffV;
-  Bars2* bars = reinterpret_cast<Bars2*>(base + kP2OffBar);
-  volatile int* abort = &bars->abort;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 2);  // one arrival per MMA warp
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->k_full[i], 1);
-      mbar_init(&bars->k_empty[i], 2);
-      mbar_init(&bars->v_full[i], 1);
-      mbar_init(&bars->v_empty[i], 2);
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], 4);
-      mbar_init(&bars->pv_done[i], 1);
-      mbar_init(&bars->drain[i], 1);
-    }
-    bars->abort = 0;
-    fence_barrier_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_map(&tm_q);
-    tma_prefetch_map(&tm_k);
-    tma_prefetch_map(&tm_v);
-  }
-  if (warp == 2) {
-    tmem_alloc(&bars->tmem_slot, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_slot;
-  pdl_wait_primary();  // the plan kernel's item list
-  const int n_items = p.hdr[0];
-
-  if (warp < 4) {
-    regs_shrink<kP2RegsLow>();  // each register budget dominates its warpgroup's code
-  if (warp < 2) {
-    // ------------------------------------------------------------- producers
-    const bool is_v = warp == 1;
-    uint32_t it_ctr = 0, kv_ctr = 0;
-    PItem2 nxt = prefill_item2_or_empty(p, blockIdx.x, n_items);
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++it_ctr) {
-      const PItem2 I = nxt;
-      nxt = prefill_item2_or_empty(p, it + gridDim.x, n_items);
-      if (!is_v) {
-        if (!warp_mbar_wait(&bars->q_empty, (it_ctr & 1u) ^ 1u, abort, p.status)) break;
-        if (lane == 0) {
-          const bool two = I.rows1 > 0;
-          mbar_arrive_expect_tx(&bars->q_full, kTileBytes * (two ? 2u : 1u));
-          tma_load_3d(sQ, &tm_q, 0, I.h, I.q0, &bars->q_full);
-          tma_load_3d(sQ + kHalf, &tm_q, 64, I.h, I.q0, &bars->q_full);
-          if (two) {
-            tma_load_3d(sQ + kTileBytes, &tm_q, 0, I.h, I.q0 + kBM, &bars->q_full);
-            tma_load_3d(sQ + kTileBytes + kHalf, &tm_q, 64, I.h, I.q0 + kBM, &bars->q_full);
-          }
-        }
-        __syncwarp();
-      }
-      bool ok = true;
-      for (int j = 0; j < I.n && ok; ++j, ++kv_ctr) {
-        const int slot = kv_ctr & 1;
-        const uint32_t par = ((kv_ctr >> 1) & 1u) ^ 1u;
-        const TileBox box = tile_box(p, I.pbase, I.need, j, lane);
-        if (!is_v) {
-          ok = warp_mbar_wait(&bars->k_empty[slot], par, abort, p.status);
-          if (ok) load_kv_tile(p, box, &tm_k, I.g, sK + slot * kTileBytes, &bars->k_full[slot], lane);
-        } else {
-          ok = warp_mbar_wait(&bars->v_empty[slot], par, abort, p.status);
-          if (ok) load_kv_tile(p, box, &tm_v, I.g, sV + slot * kTileBytes, &bars->v_full[slot], lane);
-        }
-      }
-      if (!ok) break;
-    }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------------ MMA
-    // Stream X: S = Q_X K_j^T into its S columns; its softmax warpgroup writes
-    // P over S; O_X += P V_j. One S buffer per stream, so S of the next tile
-    // waits for the previous P V product; the other stream fills the gap.
-    const int X = warp - 2;
-    constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, 1);
-    const uint32_t sKa = smem_u32(sK), sVa = smem_u32(sV);
-    const uint64_t dq = sw128_desc(smem_u32(sQ) + X * kTileBytes, 16, 1024);
-    const uint32_t tS = tmem + X * 256, tO = tS + 128;
-    uint32_t it_ctr = 0, kv_ctr = 0, t_ctr = 0;
-    bool ok = true;
-    PItem2 nxt = prefill_item2_or_empty(p, blockIdx.x, n_items);
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++it_ctr) {
-      const PItem2 I = nxt;
-      nxt = prefill_item2_or_empty(p, it + gridDim.x, n_items);
-      const int nX = X ? I.nkv1 : I.nkv0;
-      ok = warp_mbar_wait(&bars->q_full, it_ctr & 1u, abort, p.status);
-      if (!ok) break;
-      tc_fence_after();
-      int t_item = 0;
-      for (int j = 0; j < I.n; ++j, ++kv_ctr) {
-        const int slot = kv_ctr & 1;
-        const uint32_t par = (kv_ctr >> 1) & 1u;
-        ok = warp_mbar_wait(&bars->k_full[slot], par, abort, p.status);
-        if (!ok) break;
-        if (j < nX) {
-          // the S columns hold P of the previous tile until its P V completes
-          if (t_ctr > 0) {
-            ok = warp_mbar_wait(&bars->pv_done[X], (t_ctr - 1) & 1u, abort, p.status);
-            if (!ok) break;
-          }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint64_t dk = sw128_desc(sKa + slot * kTileBytes, 16, 1024);
-#pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint32_t off = (kk / 4) * kHalf + (kk % 4) * 32;
-              tc_mma_f16(tS, desc_advance(dq, off), desc_advance(dk, off), idesc_s, kk > 0);
-            }
-            tc_commit(&bars->s_full[X]);
-            tc_commit(&bars->k_empty[slot]);
-            if (j == nX - 1) tc_commit(&bars->q_empty);
-          }
-          __syncwarp();
-          ok = warp_mbar_wait(&bars->p_full[X], t_ctr & 1u, abort, p.status) &&
-               warp_mbar_wait(&bars->v_full[slot], par, abort, p.status);
-          if (!ok) break;
-          // keys past kv_len in the request's last tile: zero their V rows so that
-          // stale values cannot reach O through a zero weight (both streams may
-          // write the same zeros)
-          const int valid = I.kv - j * kBN;
-          if (valid < kBN) {
-            const uint32_t vt = sVa + slot * kTileBytes;
-            for (int i = lane; i < (kBN - valid) * 16; i += 32) {
-              const int rr = valid + i / 16, c16 = i % 16;
-              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vt + (c16 / 8) * kHalf + rr * 128 +
-                                                                          (c16 % 8) * 16),
-                           "r"(0)
-                           : "memory");
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint64_t dv = sw128_desc(sVa + slot * kTileBytes, kHalf, 1024);
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              tc_mma_f16_tmem_a(tO, tS + 8 * kk, desc_advance(dv, kk * 2048), idesc_pv,
-                                (t_item > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(&bars->pv_done[X]);
-            tc_commit(&bars->v_empty[slot]);
-          }
-          __syncwarp();
-          ++t_ctr;
-          ++t_item;
-        } else {
-          // a tile only the other stream uses: give back this stream's share
-          if (lane == 0) mbar_arrive(&bars->k_empty[slot]);
-          ok = warp_mbar_wait(&bars->v_full[slot], par, abort, p.status);
-          if (!ok) break;
-          if (lane == 0) mbar_arrive(&bars->v_empty[slot]);
-          __syncwarp();
-        }
-      }
-      if (!ok) break;
-      if (nX == 0 && lane == 0) mbar_arrive(&bars->q_empty);
-      __syncwarp();
-    }
-    // all MMAs of this thread complete before TMEM is released
-    if (lane == 0) {
-      tc_commit(&bars->drain[X]);
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&bars->drain[X], 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
-      }
-    }
-    __syncwarp();
-  }
-  } else {
-    regs_grow<kP2RegsHigh>();
-    // --------------------------------------------------- softmax / epilogue
-    const int X = warp >= 8 ? 1 : 0;
-    const int wq = warp & 3;
-    const int row = wq * 32 + lane;
-    const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16) + X * 256;  // S at +0, O at +128
-    uint32_t t_ctr = 0;
-    bool ok = true;
-    PItem2 nxt = prefill_item2_or_empty(p, blockIdx.x, n_items);
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const PItem2 I = nxt;
-      nxt = prefill_item2_or_empty(p, it + gridDim.x, n_items);
-      const int nX = X ? I.nkv1 : I.nkv0;
-      const int rowsX = X ? I.rows1 : I.rows0;
-      if (rowsX == 0) continue;
-      const int q0 = I.q0 + X * kBM;
-      const int lim = I.kv - I.qo_len + (I.qt0 + X) * kBM + row;  // last key this row may see (causal)
-      // l: sum of the bf16-rounded weights that enter P V (normalises O so its
-      // weights sum to one); l_exact: sum of the unrounded weights (for the lse)
-      float m = -INFINITY, l = 0.f, l_exact = 0.f;
-      for (int j = 0; j < nX; ++j) {
-        ok = warp_mbar_wait(&bars->s_full[X], t_ctr & 1u, abort, p.status);
-        if (!ok) break;
-        tc_fence_after();
-        const int k0 = j * kBN;
-        int ncol = min(kBN, I.kv - k0);
-        if (p.causal) ncol = min(ncol, lim - k0 + 1);
-        uint32_t v[kBN];
-        tmem_ld32(t_lane + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
-        tmem_ld32(t_lane + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        tmem_ld32(t_lane + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
-        tmem_ld32(t_lane + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
-        tmem_wait_ld();
-        const bool full_tile = __all_sync(0xffffffffu, ncol >= kBN);
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (full_tile) {
-#pragma unroll
-          for (int e = 0; e < kBN; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(v[e]));
-        } else {
-#pragma unroll
-          for (int e = 0; e < kBN; ++e) {
-            const float x = __uint_as_float(v[e]);
-            mx[e & 3] = fmaxf(mx[e & 3], e < ncol ? x : -INFINITY);
-          }
-        }
-        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        float m_new = m;
-        bool rescale = false;
-        if (mt > -INFINITY) {
-          const float ms = mt * p.scale_log2;
-          if (m == -INFINITY) {
-            m_new = ms;
-          } else if (ms > m + kRescaleThreshold) {
-            m_new = ms;
-            rescale = true;
-          }
-        }
-        // warp-uniform rescale of this warp's O rows after the previous P V
-        if (__any_sync(0xffffffffu, rescale)) {
-          ok = warp_mbar_wait(&bars->pv_done[X], (t_ctr - 1) & 1u, abort, p.status);
-          if (!ok) break;
-          tc_fence_after();
-          const float alpha = rescale ? exp2f(m - m_new) : 1.0f;
-          l *= alpha;
-          l_exact *= alpha;
-#pragma unroll
-          for (int c = 0; c < kD / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(t_lane + 128 + c * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(t_lane + 128 + c * 32, o);
-          }
-          tmem_wait_st();
-        }
-        m = m_new;
-        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m, -m);
-        float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        float2 le2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        uint32_t w[kBN / 2];
-#pragma unroll
-        for (int e = 0; e < kBN; e += 2) {
-          float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nm2);
-          if (!full_tile) {
-            x.x = e < ncol ? x.x : -INFINITY;
-            x.y = e + 1 < ncol ? x.y : -INFINITY;
-          }
-          const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          const uint32_t pk = pack_bf16x2(pe.x, pe.y);
-          w[e / 2] = pk;
-          ls2[(e / 2) & 1] = fadd2(ls2[(e / 2) & 1], make_float2(bf16_lo(pk), bf16_hi(pk)));
-          le2[(e / 2) & 1] = fadd2(le2[(e / 2) & 1], pe);
-        }
-        l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
-        l_exact += (le2[0].x + le2[0].y) + (le2[1].x + le2[1].y);
-        tmem_st32(t_lane + 0, *reinterpret_cast<uint32_t(*)[32]>(w + 0));
-        tmem_st32(t_lane + 32, *reinterpret_cast<uint32_t(*)[32]>(w + 32));
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->p_full[X]);
-        ++t_ctr;
-      }
-      if (!ok) break;
-      // ---- epilogue: O / l and the log-sum-exp, once the last P V is done
-      if (nX > 0) {
-        ok = warp_mbar_wait(&bars->pv_done[X], (t_ctr - 1) & 1u, abort, p.status);
-        if (!ok) break;
-        tc_fence_after();
-      }
-      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-      const bool store = row < rowsX;
-      const int64_t orow = ((int64_t)(q0 + row) * p.hq + I.h) * kD;
-      uint32_t v[kD];
-      if (nX > 0) {
-        tmem_ld32(t_lane + 128, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
-        tmem_ld32(t_lane + 160, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        tmem_ld32(t_lane + 192, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
-        tmem_ld32(t_lane + 224, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int e = 0; e < kD; ++e) v[e] = 0u;
-      }
-      if (store) {
-        if (p.o_dtype == PD_BF16) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow);
-#pragma unroll
-          for (int k = 0; k < kD / 8; ++k) {
-            uint4 u;
-            u.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l);
-            u.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l);
-            u.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l);
-            u.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l);
-            dst[k] = u;
-          }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow);
-#pragma unroll
-          for (int k = 0; k < kD / 4; ++k)
-            dst[k] = make_float4(__uint_as_float(v[4 * k]) * inv_l, __uint_as_float(v[4 * k + 1]) * inv_l,
-                                 __uint_as_float(v[4 * k + 2]) * inv_l, __uint_as_float(v[4 * k + 3]) * inv_l);
-        }
-        if (p.lse != nullptr)
-          p.lse[(int64_t)(q0 + row) * p.hq + I.h] =
-              (nX > 0 && l_exact > 0.f) ? (m + log2f(l_exact)) * kLn2 : -INFINITY;
-      }
-      tc_fence_before();
-    }
-  }
-
-  // Normally every copy has been consumed here. After an abort, copies may still
-  // be in flight: give them a bounded 2 ms to land before shared memory is freed.
-  if (*abort && warp == 0 && lane == 0) {
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 2000000ull) {
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------- host
@@ -1078,17 +701,11 @@ int prefill_supported(int32_t kv_dtype, int32_t head_dim, int32_t page_size) {
   return PD_OK;
 }
 
-// 1: items of two q tiles on the two-pipeline kernel; 0: one q tile per item.
-#ifndef PD_PREFILL_PAIR
-#define PD_PREFILL_PAIR 0
-#endif
-
 int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const void* v_pool, cudaStream_t stream) {
-  p.pair = PD_PREFILL_PAIR;
   CUtensorMap tq, tk, tv, to;
   const int pb = p.page_size < kBN ? p.page_size : kBN;
   memset(&to, 0, sizeof(to));
-  if (!p.pair && p.o_dtype == PD_BF16 && !make_rows_map(&to, p.o, PD_BF16, p.total_qo, p.hq, kD, 64, kBM, true))
+  if (p.o_dtype == PD_BF16 && !make_rows_map(&to, p.o, PD_BF16, p.total_qo, p.hq, kD, 64, kBM, true))
     return PD_ERR_CUDA;
   if (!make_rows_map(&tq, q, PD_BF16, p.total_qo, p.hq, kD, 64, kBM, true) ||
       !make_pool_map(&tk, k_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true) ||
@@ -1099,23 +716,21 @@ int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const vo
   if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;
   if (configured_device != dev) {
     if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrefillSmem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(prefill2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kP2Smem) !=
-            cudaSuccess)
+        cudaSuccess)
       return PD_ERR_CUDA;
     configured_device = dev;
   }
   prefill_plan_kernel<<<1, 1024, 0, stream>>>(p);
   int64_t grid = device_sm_count();
-  const int64_t max_items = (int64_t)(p.pair ? (p.max_rq + 1) / 2 + p.batch : p.max_rq) * p.hq;
+  const int64_t max_items = (int64_t)p.max_rq * p.hq;
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
   // A programmatic dependent of the plan (CTAs set up while it finishes),
   // except when timed alone through the profiling events.
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(p.pair ? kThreadsP2 : kThreadsPf);
-  cfg.dynamicSmemBytes = p.pair ? kP2Smem : kPrefillSmem;
+  cfg.blockDim = dim3(kThreadsPf);
+  cfg.dynamicSmemBytes = kPrefillSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1123,8 +738,7 @@ int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const vo
   cfg.attrs = attr;
   cfg.numAttrs = profile_events().start != nullptr ? 0 : 1;
   profile_begin(stream);
-  const cudaError_t e = p.pair ? cudaLaunchKernelEx(&cfg, prefill2_kernel, tq, tk, tv, p)
-                               : cudaLaunchKernelEx(&cfg, prefill_kernel, tq, tk, tv, to, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_kernel, tq, tk, tv, to, p);
   profile_end(stream);
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
 }
