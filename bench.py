@@ -343,6 +343,25 @@ def measure_rows(args, dev, peaks) -> dict:
         rows["prefill"] = {"status": str(e)}
     del w
 
+    # a compute-bound causal prefill (same kernel): long sequences put the
+    # arithmetic intensity above the GB300 ridge
+    B2, L2, H2 = 2, 8192, 16
+    w = torch_gen.paged_batch(3, [L2] * B2, [L2] * B2, H2, H2, 128, 16, device=dev)
+    flops2 = 2 * 128 * L2 * (L2 + 1) * H2 * B2
+    try:
+        o = torch.empty_like(w["q"])
+        ms, kms, hus = timed(lambda: pd.pd_attn_prefill(w["q"], w["k_pool"], w["v_pool"], w["kv_len"],
+                                                        w["page_indptr"], w["page_indices"], w["qo_indptr"],
+                                                        max_qo_len=L2, max_kv_len=L2, o=o), reps, warm, flush)
+        t = flops2 / (kms * 1e-3) / 1e12
+        rows["prefill_long"] = {"workload": "2 x 8192 causal, 16 heads, D 128, page 16, bf16", "ms": round(ms, 5),
+                                "kernel_ms": round(kms, 5), "host_us": round(hus, 1), "TFLOPs": round(t, 1),
+                                "frac_bf16": round(t / peaks["bf16"], 4), "bound": "tensor (2048 flop/B > ridge)",
+                                "flops": flops2}
+    except pd.PdError as e:
+        rows["prefill_long"] = {"status": str(e)}
+    del w
+
     w = torch_gen.mixed_1p_nd(device=dev)
     kvb = int(w["kv_len_host"].sum()) * 40 * 128 * 2 * 2 + 2 * w["q"].numel() * 2
     pre = int(w["qo_len_host"][0])

@@ -122,3 +122,19 @@ def test_prefill_deterministic():
     a, la = run_prefill(case, torch.bfloat16)
     b, lb = run_prefill(case, torch.bfloat16)
     assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+def test_long_causal_prefill_sampled_rows():
+    # 2 x 4096 causal, GQA 8/2: items of up to 32 KV tiles; rows sampled across
+    # both requests (first, last and random rows) and checked one by one
+    case = wl.make_attn_case(307, [4096, 4096], [4096, 4096], 8, 2, 128, 16, wl.BF16, causal=True)
+    o, lse = run_prefill(case)
+    rng = np.random.default_rng(307)
+    rows = np.concatenate([[0, 127, 128, 4095, 4096, 8191], rng.integers(0, 8192, size=58)])
+    heads = rng.integers(0, 8, size=rows.size)
+    o_ref, lse_ref = oracle.attention_rows(case.qo_indptr, case.kv_len, case.table.page_indptr,
+                                           case.table.page_indices, case.q, case.k_pool, case.v_pool, 8, 2,
+                                           case.scale, rows, heads, causal=True)
+    got = host_f64(o)[rows, heads]
+    assert float(np.abs(got - o_ref).max()) <= 1e-2
+    assert float(np.abs(lse.cpu().numpy()[rows, heads] - lse_ref).max()) <= LSE_TOL
