@@ -132,18 +132,9 @@ __device__ __forceinline__ bool warp_mbar_wait(uint64_t* bar, uint32_t parity, v
 }
 
 // -------------------------------------------------------- bulk async copies
-// Global -> shared copy by the TMA engine; completion is counted in bytes on `bar`.
+// Global -> shared copy by the TMA engine with an L2 eviction-priority hint
+// (policy from make_evict_first()); completion is counted in bytes on `bar`.
 // Addresses 16-byte aligned, size a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Same, with an L2 eviction-priority hint (policy from make_evict_first()).
 __device__ __forceinline__ void bulk_g2s_hint(void* smem_dst, const void* gmem_src, uint32_t bytes,
                                               uint64_t* bar, uint64_t policy) {
   asm volatile(
@@ -151,19 +142,6 @@ __device__ __forceinline__ void bulk_g2s_hint(void* smem_dst, const void* gmem_s
       "%2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
       "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
-}
-
-// 16-byte asynchronous copy global -> shared by this thread (L2 hint policy).
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, uint64_t policy) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
-               "l"(gmem_src), "l"(policy)
-               : "memory");
-}
-
-// Arrives on `bar` once every cp.async this thread issued so far has landed; the
-// arrival is one of the barrier's expected arrivals (no pending-count increment).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ uint64_t make_evict_first() {
@@ -183,16 +161,22 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
   return r;
 }
 
+// d = a * b + c on a pair of fp32 values with one packed instruction.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 // Two fp32 values -> one bf16x2 word, `lo` in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
-}
-
-__device__ __forceinline__ int named_barrier_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-  return 0;
 }
 
 }  // namespace pd

@@ -126,17 +126,6 @@ __device__ __forceinline__ void load_lane_row(const uint8_t* row, int dg, float 
   }
 }
 
-// d = a * b + c on a pair of fp32 values with one packed instruction.
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-
 template <int ES, int D>
 __device__ __forceinline__ int lane_dim(int dg, int e) {
   using G = Geo<ES, D>;

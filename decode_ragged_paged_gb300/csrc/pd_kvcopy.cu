@@ -209,12 +209,9 @@ namespace {
 int copy_grid() { return device_sm_count() * (2048 / kCopyThreads); }
 }  // namespace
 
-#ifndef PD_APPEND_ONE_ROW_PER_CTA
-#define PD_APPEND_ONE_ROW_PER_CTA 0
-#endif
 int launch_kv_append(const KvCopyParams& p, cudaStream_t stream) {
   if (p.max_new <= 0 || p.batch <= 0) return PD_OK;
-  int grid = PD_APPEND_ONE_ROW_PER_CTA ? p.max_new : copy_grid();
+  int grid = copy_grid();
   if (grid > p.max_new) grid = p.max_new;
   profile_begin(stream);
   kv_append_kernel<<<grid, kCopyThreads, 0, stream>>>(p);
