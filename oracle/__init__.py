@@ -63,9 +63,9 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
             lib.oracle_attention_rows.argtypes = [I32, P, P, P, P, I32, I32, I32, I32, I32, D, I32,
                                                   P, P, P, I64, P, P, P, P, I32]
             lib.oracle_kv_append.argtypes = [I32, P, P, P, P, I32, I32, I32, I32, I32, P, P, P, P]
-            lib.oracle_kv_pack.argtypes = [I32, P, P, P, I32, I32, I64, I32, I32, I32, I32,
+            lib.oracle_kv_pack.argtypes = [I32, P, P, P, I32, I32, I64, I32, I32, I32, I32, I32, I32,
                                            P, P, P, P]
-            lib.oracle_kv_unpack.argtypes = [I32, P, P, P, I32, I32, I64, I32, I32, I32, I32,
+            lib.oracle_kv_unpack.argtypes = [I32, P, P, P, I32, I32, I64, I32, I32, I32, I32, I32, I32,
                                              P, P, P, P]
             lib.oracle_num_threads.argtypes = [I32]
             for f in ("oracle_attention", "oracle_attention_rows", "oracle_kv_append",
@@ -157,25 +157,30 @@ def kv_append(new_indptr, kv_len, page_indptr, page_indices, k_new, v_new, k_poo
         raise ValueError("oracle_kv_append rejected its inputs")
 
 
-def kv_pack(kv_len, page_indptr, page_indices, k_pools, v_pools, dst_offsets, dst_bytes, mutant=0):
-    """k_pools / v_pools: [L][num_pages][Hkv][P][D]. Returns the packed uint8 buffer."""
+def kv_pack(kv_len, page_indptr, page_indices, k_pools, v_pools, dst_offsets, dst_bytes, mutant=0,
+            head_begin=0, head_count=None):
+    """k_pools / v_pools: [L][num_pages][Hkv][P][D]. Returns the packed uint8 buffer holding heads
+    [head_begin, head_begin + head_count) (all heads by default)."""
     kv_len = _i32(kv_len)
     page_indptr, page_indices = _i32(page_indptr), _i32(page_indices)
     k_pools, v_pools = np.ascontiguousarray(k_pools), np.ascontiguousarray(v_pools)
     dst_offsets = np.ascontiguousarray(dst_offsets, dtype=np.int64)
     L, num_pages, hkv, p, d = k_pools.shape
     stride = k_pools[0].nbytes
+    head_count = hkv - head_begin if head_count is None else head_count
     dst = np.zeros(int(dst_bytes), dtype=np.uint8)
     rc = _load(mutant).oracle_kv_pack(len(kv_len), _ptr(kv_len), _ptr(page_indptr), _ptr(page_indices),
-                                      num_pages, L, stride, hkv, d, p, k_pools.itemsize,
+                                      num_pages, L, stride, hkv, head_begin, head_count, d, p, k_pools.itemsize,
                                       _ptr(k_pools), _ptr(v_pools), _ptr(dst), _ptr(dst_offsets))
     if rc != 0:
         raise ValueError("oracle_kv_pack rejected its inputs")
     return dst
 
 
-def kv_unpack(kv_len, page_indptr, page_indices, src, src_offsets, k_pools, v_pools, mutant=0):
-    """In-place unpack of the packed uint8 buffer ``src`` into [L][num_pages][Hkv][P][D] pools."""
+def kv_unpack(kv_len, page_indptr, page_indices, src, src_offsets, k_pools, v_pools, mutant=0,
+              head_begin=0, head_count=None):
+    """In-place unpack of the packed uint8 buffer ``src`` (holding head_count heads) into heads
+    [head_begin, head_begin + head_count) of [L][num_pages][Hkv][P][D] pools (all heads by default)."""
     kv_len = _i32(kv_len)
     page_indptr, page_indices = _i32(page_indptr), _i32(page_indices)
     src = np.ascontiguousarray(src)
@@ -183,8 +188,9 @@ def kv_unpack(kv_len, page_indptr, page_indices, src, src_offsets, k_pools, v_po
     assert k_pools.flags["C_CONTIGUOUS"] and v_pools.flags["C_CONTIGUOUS"]
     L, num_pages, hkv, p, d = k_pools.shape
     stride = k_pools[0].nbytes
+    head_count = hkv - head_begin if head_count is None else head_count
     rc = _load(mutant).oracle_kv_unpack(len(kv_len), _ptr(kv_len), _ptr(page_indptr), _ptr(page_indices),
-                                        num_pages, L, stride, hkv, d, p, k_pools.itemsize,
+                                        num_pages, L, stride, hkv, head_begin, head_count, d, p, k_pools.itemsize,
                                         _ptr(src), _ptr(src_offsets), _ptr(k_pools), _ptr(v_pools))
     if rc != 0:
         raise ValueError("oracle_kv_unpack rejected its inputs")

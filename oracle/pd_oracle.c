@@ -331,23 +331,46 @@ static int64_t packed_row_bytes(int layer, int kv, int h, int64_t t, int64_t n, 
  *   dst[dst_offsets[r] + packed(layer, kv, h, t)] = pool_layer,kv[page(r, t)][h][t % p]
  * where layer l's pools start at k_pool / v_pool + l * layer_stride bytes.
  */
+/*
+ * Head range (same post, "Sharded KV cache transfers": when prefiller and
+ * decoder shard the heads differently, pages are split or rebuilt): pack and
+ * unpack move heads [head_begin, head_begin + head_count) of a pool holding hkv
+ * heads; the block then holds head_count heads, [layer][K,V][head_count][kv_len]
+ * [head_dim]. The full range (0, hkv) is the plain handoff.
+ */
+static int head_range_ok(int32_t hkv, int32_t head_begin, int32_t head_count) {
+  return head_begin >= 0 && head_count >= 1 && head_begin + head_count <= hkv;
+}
+
+/* pool head that packed head h of the range maps to */
+static int pool_head(int32_t head_begin, int h) {
+#if ORACLE_MUTANT == 11
+  (void)head_begin;
+  return h; /* planted: the range's offset into the pool is dropped */
+#else
+  return head_begin + h;
+#endif
+}
+
 int oracle_kv_pack(int32_t batch, const int32_t *kv_len, const int32_t *page_indptr,
                    const int32_t *page_indices, int32_t num_pages, int32_t num_layers,
-                   int64_t layer_stride, int32_t hkv, int32_t d, int32_t p, int32_t es,
-                   const void *k_pool, const void *v_pool, void *dst, const int64_t *dst_offsets) {
+                   int64_t layer_stride, int32_t hkv, int32_t head_begin, int32_t head_count, int32_t d,
+                   int32_t p, int32_t es, const void *k_pool, const void *v_pool, void *dst,
+                   const int64_t *dst_offsets) {
   const int64_t row_bytes = (int64_t)d * es;
+  if (!head_range_ok(hkv, head_begin, head_count)) return -1;
   for (int r = 0; r < batch; ++r) {
     const int64_t n = kv_len[r];
     if ((int64_t)(page_indptr[r + 1] - page_indptr[r]) * p < n) return -1;
     for (int layer = 0; layer < num_layers; ++layer)
       for (int kv = 0; kv < 2; ++kv) {
         const char *pool = (const char *)(kv ? v_pool : k_pool) + (int64_t)layer * layer_stride;
-        for (int h = 0; h < hkv; ++h)
+        for (int h = 0; h < head_count; ++h)
           for (int64_t t = 0; t < n; ++t) {
             const int64_t page = page_indices[page_indptr[r] + t / p];
             if (page < 0 || page >= num_pages) return -1;
-            const int64_t src = pool_row_bytes(page, h, (int)(t % p), hkv, p, d, es);
-            const int64_t out = dst_offsets[r] + packed_row_bytes(layer, kv, h, t, n, hkv, d, es);
+            const int64_t src = pool_row_bytes(page, pool_head(head_begin, h), (int)(t % p), hkv, p, d, es);
+            const int64_t out = dst_offsets[r] + packed_row_bytes(layer, kv, h, t, n, head_count, d, es);
             memcpy((char *)dst + out, pool + src, (size_t)row_bytes);
           }
       }
@@ -361,9 +384,11 @@ int oracle_kv_pack(int32_t batch, const int32_t *kv_len, const int32_t *page_ind
  */
 int oracle_kv_unpack(int32_t batch, const int32_t *kv_len, const int32_t *page_indptr,
                      const int32_t *page_indices, int32_t num_pages, int32_t num_layers,
-                     int64_t layer_stride, int32_t hkv, int32_t d, int32_t p, int32_t es,
-                     const void *src, const int64_t *src_offsets, void *k_pool, void *v_pool) {
+                     int64_t layer_stride, int32_t hkv, int32_t head_begin, int32_t head_count, int32_t d,
+                     int32_t p, int32_t es, const void *src, const int64_t *src_offsets, void *k_pool,
+                     void *v_pool) {
   const int64_t row_bytes = (int64_t)d * es;
+  if (!head_range_ok(hkv, head_begin, head_count)) return -1;
   for (int r = 0; r < batch; ++r) {
     const int64_t n = kv_len[r];
     if ((int64_t)(page_indptr[r + 1] - page_indptr[r]) * p < n) return -1;
@@ -374,13 +399,13 @@ int oracle_kv_unpack(int32_t batch, const int32_t *kv_len, const int32_t *page_i
 #else
         char *pool = (char *)(kv ? v_pool : k_pool) + (int64_t)layer * layer_stride;
 #endif
-        for (int h = 0; h < hkv; ++h)
+        for (int h = 0; h < head_count; ++h)
           for (int64_t t = 0; t < n; ++t) {
             const int64_t page = page_indices[page_indptr[r] + t / p];
             if (page < 0 || page >= num_pages) return -1;
             const int slot = (int)(t % p);
-            const int64_t dst = pool_row_bytes(page, h, slot, hkv, p, d, es);
-            const int64_t in = src_offsets[r] + packed_row_bytes(layer, kv, h, t, n, hkv, d, es);
+            const int64_t dst = pool_row_bytes(page, pool_head(head_begin, h), slot, hkv, p, d, es);
+            const int64_t in = src_offsets[r] + packed_row_bytes(layer, kv, h, t, n, head_count, d, es);
             memcpy(pool + dst, (const char *)src + in, (size_t)row_bytes);
           }
       }

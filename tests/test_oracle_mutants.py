@@ -23,6 +23,7 @@ MUTANTS = {
     8: "packed block token-major",
     9: "unpack writes K into the V pool",
     10: "append writes new tokens in reverse order",
+    11: "head range packed from the pool's first heads",
 }
 
 
@@ -68,6 +69,17 @@ def _copy_pins_hold(mutant):
                            kd, vd, hc.dst_offsets, total, mutant=0)
     if not np.array_equal(buf, again):
         return False
+    # a head range is the head slice of the full block
+    part_total = wl.packed_bytes(hc.kv_len, 2, 1, 4, 4)
+    part_off = np.array([0, wl.packed_bytes(hc.kv_len[:1], 2, 1, 4, 4)], np.int64)
+    part = oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices,
+                          hc.k_src, hc.v_src, part_off, part_total, mutant=mutant, head_begin=1, head_count=1)
+    for r, n in enumerate(hc.kv_len):
+        full_r = buf[hc.dst_offsets[r]:hc.dst_offsets[r] + wl.packed_bytes([n], 2, 2, 4, 4)]
+        want = full_r.reshape(2, 2, 2, n, 16)[:, :, 1:2]
+        got = part[part_off[r]:part_off[r] + want.size].reshape(want.shape)
+        if not np.array_equal(got, want):
+            return False
     pre = wl.make_attn_case(82, [5, 3], [9, 12], 2, 2, 4, 4, wl.F32, with_new_tokens=True, num_pages=8)
     full = wl.make_attn_case(82, [5, 3], [9, 12], 2, 2, 4, 4, wl.F32, with_new_tokens=False, num_pages=8)
     k2, v2 = pre.k_pool.copy(), pre.v_pool.copy()

@@ -357,3 +357,72 @@ def test_transfer_estimate_bookkeeping():
     ms = total / (g["links"][0] * g["link_gib_s"][0] * 2 ** 30) * 1e3
     assert ms == pytest.approx(g["transfer_ms"][0], abs=1e-9)
     assert round(ms, 1) == g["printed_ms"][0]
+
+
+def _block_heads(buf, off, n, layers, heads, row_bytes):
+    """One request's packed block as [layer][K,V][head][token][row bytes]."""
+    size = layers * 2 * heads * n * row_bytes
+    return buf[off:off + size].reshape(layers, 2, heads, n, row_bytes)
+
+
+def test_head_range_pack_is_the_head_slice_of_the_full_pack():
+    # Perplexity, "Disaggregated prefill and decode" (2025), "Sharded KV cache
+    # transfers": a shard's heads are a slice of the whole, so packing heads
+    # [h0, h0 + hc) must give exactly that slice of the full block.
+    hc = wl.kv_handoff(seed=91, batch=3, layers=2, heads=4, head_dim=8, src_page=4, dst_page=8,
+                       dtype=wl.BF16, kv_lens=[9, 16, 5])
+    row = 8 * 2
+    full = oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, hc.k_src, hc.v_src,
+                          hc.dst_offsets, wl.packed_bytes(hc.kv_len, 2, 4, 8, 2))
+    for h0, cnt in [(0, 4), (1, 2), (3, 1)]:
+        per = np.asarray(hc.kv_len, np.int64) * 2 * 2 * cnt * row
+        offs = np.concatenate([[0], np.cumsum(per)[:-1]]).astype(np.int64)
+        part = oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, hc.k_src,
+                              hc.v_src, offs, int(per.sum()), head_begin=h0, head_count=cnt)
+        for r, n in enumerate(hc.kv_len):
+            want = _block_heads(full, hc.dst_offsets[r], n, 2, 4, row)[:, :, h0:h0 + cnt]
+            assert np.array_equal(_block_heads(part, offs[r], n, 2, cnt, row), want)
+
+
+def test_tp2_prefiller_to_tp1_decoder_and_back():
+    # Two prefiller shards hold heads [0, 2) and [2, 4) of the same logical pool;
+    # each packs its own pool and the decoder unpacks both into one 4-head pool
+    # at head offsets 0 and 2: the result equals unpacking the whole at once.
+    # Back the other way, head ranges of the decoder pool unpacked into 2-head
+    # pools give the head slices of the whole.
+    hc = wl.kv_handoff(seed=92, batch=2, layers=2, heads=4, head_dim=8, src_page=4, dst_page=8,
+                       dtype=wl.BF16, kv_lens=[11, 20])
+    full_bytes = wl.packed_bytes(hc.kv_len, 2, 4, 8, 2)
+    half_bytes = wl.packed_bytes(hc.kv_len, 2, 2, 8, 2)
+    half_offs = (hc.dst_offsets // 2).astype(np.int64)
+    dshape = (2, hc.dst_table.num_pages, 4, 8, 8)
+    ref_k, ref_v = np.full(dshape, 0xFFFF, np.uint16), np.full(dshape, 0xFFFF, np.uint16)
+    whole = oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, hc.k_src, hc.v_src,
+                           hc.dst_offsets, full_bytes)
+    oracle.kv_unpack(hc.kv_len, hc.dst_table.page_indptr, hc.dst_table.page_indices, whole, hc.dst_offsets,
+                     ref_k, ref_v)
+    k1, v1 = np.full(dshape, 0xFFFF, np.uint16), np.full(dshape, 0xFFFF, np.uint16)
+    for s in range(2):
+        ks = np.ascontiguousarray(hc.k_src[:, :, 2 * s:2 * s + 2])
+        vs = np.ascontiguousarray(hc.v_src[:, :, 2 * s:2 * s + 2])
+        buf = oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, ks, vs,
+                             half_offs, half_bytes)
+        oracle.kv_unpack(hc.kv_len, hc.dst_table.page_indptr, hc.dst_table.page_indices, buf, half_offs,
+                         k1, v1, head_begin=2 * s, head_count=2)
+    assert np.array_equal(k1, ref_k) and np.array_equal(v1, ref_v)
+    for s in range(2):
+        buf = oracle.kv_pack(hc.kv_len, hc.dst_table.page_indptr, hc.dst_table.page_indices, ref_k, ref_v,
+                             half_offs, half_bytes, head_begin=2 * s, head_count=2)
+        hshape = (2, hc.dst_table.num_pages, 2, 8, 8)
+        k2, v2 = np.full(hshape, 0xFFFF, np.uint16), np.full(hshape, 0xFFFF, np.uint16)
+        oracle.kv_unpack(hc.kv_len, hc.dst_table.page_indptr, hc.dst_table.page_indices, buf, half_offs, k2, v2)
+        assert np.array_equal(k2, ref_k[:, :, 2 * s:2 * s + 2]) and np.array_equal(v2, ref_v[:, :, 2 * s:2 * s + 2])
+
+
+def test_head_range_outside_the_pool_is_rejected():
+    hc = wl.kv_handoff(seed=93, batch=1, layers=1, heads=2, head_dim=8, src_page=4, dst_page=8,
+                       dtype=wl.BF16, kv_lens=[5])
+    for h0, cnt in [(1, 2), (-1, 1), (0, 0)]:
+        with pytest.raises(ValueError):
+            oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, hc.k_src, hc.v_src,
+                           [0], 1024, head_begin=h0, head_count=cnt)
