@@ -411,6 +411,21 @@ def measure_rows(args, dev, peaks) -> dict:
                       "kernel_ms": round(kms, 5), "host_us": round(hus, 1),
                       "GBs": round(byts / kms / 1e6, 1), "frac_hbm": round(byts / kms / 1e6 / hbm, 4),
                       "bound": "hbm", "bytes": byts}
+    # sharded handoff (TP2 prefiller -> TP1 decoder): two blocks of 20 heads
+    # unpacked into heads [0, 20) and [20, 40) of one 40-head pool
+    half = w["buffer"][: w["buffer"].numel() // 2]
+    half_offs = w["offsets"] // 2
+
+    def unpack_tp2():
+        for s_ in range(2):
+            pd.pd_kv_unpack_heads(half, half_offs, w["k_dst"], w["v_dst"], w["kv_len"], w["dst_indptr"],
+                                  w["dst_indices"], 20 * s_, 20, max_kv_len=512)
+
+    ms, _, hus = timed(unpack_tp2, reps, warm, prof=False)
+    rows["unpack_tp2_to_tp1"] = {"workload": "two 20-head blocks into heads [0,20) and [20,40) of the page-64 pool",
+                                 "ms": round(ms, 5), "host_us": round(hus, 1), "GBs": round(byts / ms / 1e6, 1),
+                                 "frac_hbm": round(byts / ms / 1e6 / hbm, 4), "bound": "hbm", "bytes": byts,
+                                 "launches": 2}
     del w
     return rows
 

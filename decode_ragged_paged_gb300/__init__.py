@@ -35,7 +35,8 @@ DEVICE_STATUS = {0: "ok", 1: "bad indptr", 2: "bad length", 3: "bad page table",
 # Every symbol include/pd.h declares.
 EXPORTS = ("pd_attn_workspace_size", "pd_attn_decode", "pd_attn_decode_static", "pd_attn_prefill",
            "pd_attn_mixed",
-           "pd_kv_append", "pd_kv_pack", "pd_kv_unpack", "pd_profile_events", "pd_status_string",
+           "pd_kv_append", "pd_kv_pack", "pd_kv_unpack", "pd_kv_pack_heads", "pd_kv_unpack_heads",
+           "pd_profile_events", "pd_status_string",
            "pd_device_status_string", "pd_version")
 
 
@@ -86,7 +87,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.pd_kv_append.argtypes = [ctypes.POINTER(KvDesc), ctypes.POINTER(Batch), P, P, P, P, P, P]
             lib.pd_kv_pack.argtypes = [ctypes.POINTER(KvDesc), ctypes.POINTER(Batch), P, P, P, S, P, P, P]
             lib.pd_kv_unpack.argtypes = [ctypes.POINTER(KvDesc), ctypes.POINTER(Batch), P, S, P, P, P, P, P]
-            for name in ("pd_kv_append", "pd_kv_pack", "pd_kv_unpack"):
+            lib.pd_kv_pack_heads.argtypes = [ctypes.POINTER(KvDesc), ctypes.POINTER(Batch), I32, I32, P, P, P, S, P,
+                                             P, P]
+            lib.pd_kv_unpack_heads.argtypes = [ctypes.POINTER(KvDesc), ctypes.POINTER(Batch), I32, I32, P, S, P, P,
+                                               P, P, P]
+            for name in ("pd_kv_append", "pd_kv_pack", "pd_kv_unpack", "pd_kv_pack_heads", "pd_kv_unpack_heads"):
                 getattr(lib, name).restype = ctypes.c_int
             lib.pd_status_string.argtypes = [I32]
             lib.pd_status_string.restype = ctypes.c_char_p
@@ -255,6 +260,32 @@ def pd_kv_unpack(src, src_offsets, k_pools, v_pools, kv_len, page_indptr, page_i
     rc = lib.pd_kv_unpack(ctypes.byref(desc), ctypes.byref(batch), _ptr(src), src.numel() * src.element_size(),
                           _ptr(src_offsets), _ptr(k_pools), _ptr(v_pools), _ptr(dev_status), _stream(stream))
     _check(rc, "pd_kv_unpack")
+
+
+def pd_kv_pack_heads(k_pools, v_pools, kv_len, page_indptr, page_indices, dst, dst_offsets, head_begin, head_count,
+                     *, max_kv_len=None, dev_status=None, stream=None):
+    """pd_kv_pack of pool heads [head_begin, head_begin + head_count) only; blocks hold head_count heads."""
+    lib = load_library()
+    L, stride, num_pages = _layers(k_pools)
+    desc = _kv_desc(k_pools, L, stride)
+    batch = make_batch(kv_len, page_indptr, page_indices, num_pages, max_kv_len=max_kv_len)
+    rc = lib.pd_kv_pack_heads(ctypes.byref(desc), ctypes.byref(batch), int(head_begin), int(head_count),
+                              _ptr(k_pools), _ptr(v_pools), _ptr(dst), dst.numel() * dst.element_size(),
+                              _ptr(dst_offsets), _ptr(dev_status), _stream(stream))
+    _check(rc, "pd_kv_pack_heads")
+
+
+def pd_kv_unpack_heads(src, src_offsets, k_pools, v_pools, kv_len, page_indptr, page_indices, head_begin, head_count,
+                       *, max_kv_len=None, dev_status=None, stream=None):
+    """pd_kv_unpack of blocks holding head_count heads into pool heads [head_begin, head_begin + head_count)."""
+    lib = load_library()
+    L, stride, num_pages = _layers(k_pools)
+    desc = _kv_desc(k_pools, L, stride)
+    batch = make_batch(kv_len, page_indptr, page_indices, num_pages, max_kv_len=max_kv_len)
+    rc = lib.pd_kv_unpack_heads(ctypes.byref(desc), ctypes.byref(batch), int(head_begin), int(head_count),
+                                _ptr(src), src.numel() * src.element_size(), _ptr(src_offsets), _ptr(k_pools),
+                                _ptr(v_pools), _ptr(dev_status), _stream(stream))
+    _check(rc, "pd_kv_unpack_heads")
 
 
 def pd_profile_events(start=None, stop=None) -> None:

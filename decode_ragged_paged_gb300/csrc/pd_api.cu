@@ -240,6 +240,8 @@ KvCopyParams kv_params(const pd_kv_desc* d, const pd_batch* b, int32_t* status) 
   p.num_layers = d->num_layers;
   p.num_pages = b->num_pages;
   p.elem_size = elem_size(d->dtype);
+  p.head_begin = 0;
+  p.head_count = d->num_kv_heads;
   p.max_kv_len = b->max_kv_len;
   p.max_new = b->total_qo;
   p.layer_stride = d->layer_stride_bytes;
@@ -270,14 +272,18 @@ int pd_kv_append(const pd_kv_desc* desc, const pd_batch* batch, const void* k_ne
   return launch_kv_append(p, static_cast<cudaStream_t>(stream));
 }
 
-int pd_kv_pack(const pd_kv_desc* desc, const pd_batch* batch, const void* k_pool, const void* v_pool, void* dst,
-               size_t dst_bytes, const int64_t* dst_offsets, int32_t* dev_status, void* stream) {
+int pd_kv_pack_heads(const pd_kv_desc* desc, const pd_batch* batch, int32_t head_begin, int32_t head_count,
+                     const void* k_pool, const void* v_pool, void* dst, size_t dst_bytes,
+                     const int64_t* dst_offsets, int32_t* dev_status, void* stream) {
   int rc = check_kv(desc, batch);
   if (rc != PD_OK) return rc;
+  if (head_begin < 0 || head_count < 1 || head_count > desc->num_kv_heads - head_begin) return PD_ERR_INVALID_ARG;
   if (batch->batch_size == 0) return PD_OK;
   if (k_pool == nullptr || v_pool == nullptr || dst == nullptr || dst_offsets == nullptr) return PD_ERR_INVALID_ARG;
   if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(dst)) return PD_ERR_INVALID_ARG;
   KvCopyParams p = kv_params(desc, batch, dev_status);
+  p.head_begin = head_begin;
+  p.head_count = head_count;
   p.src = k_pool;
   p.src2 = v_pool;
   p.dst = dst;
@@ -286,20 +292,38 @@ int pd_kv_pack(const pd_kv_desc* desc, const pd_batch* batch, const void* k_pool
   return launch_kv_pack(p, static_cast<cudaStream_t>(stream));
 }
 
-int pd_kv_unpack(const pd_kv_desc* desc, const pd_batch* batch, const void* src, size_t src_bytes,
-                 const int64_t* src_offsets, void* k_pool, void* v_pool, int32_t* dev_status, void* stream) {
+int pd_kv_pack(const pd_kv_desc* desc, const pd_batch* batch, const void* k_pool, const void* v_pool, void* dst,
+               size_t dst_bytes, const int64_t* dst_offsets, int32_t* dev_status, void* stream) {
+  if (desc == nullptr) return PD_ERR_INVALID_ARG;
+  return pd_kv_pack_heads(desc, batch, 0, desc->num_kv_heads, k_pool, v_pool, dst, dst_bytes, dst_offsets,
+                          dev_status, stream);
+}
+
+int pd_kv_unpack_heads(const pd_kv_desc* desc, const pd_batch* batch, int32_t head_begin, int32_t head_count,
+                       const void* src, size_t src_bytes, const int64_t* src_offsets, void* k_pool, void* v_pool,
+                       int32_t* dev_status, void* stream) {
   int rc = check_kv(desc, batch);
   if (rc != PD_OK) return rc;
+  if (head_begin < 0 || head_count < 1 || head_count > desc->num_kv_heads - head_begin) return PD_ERR_INVALID_ARG;
   if (batch->batch_size == 0) return PD_OK;
   if (k_pool == nullptr || v_pool == nullptr || src == nullptr || src_offsets == nullptr) return PD_ERR_INVALID_ARG;
   if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(src)) return PD_ERR_INVALID_ARG;
   KvCopyParams p = kv_params(desc, batch, dev_status);
+  p.head_begin = head_begin;
+  p.head_count = head_count;
   p.src = src;
   p.dst = k_pool;
   p.dst2 = v_pool;
   p.offsets = src_offsets;
   p.buf_bytes = (int64_t)src_bytes;
   return launch_kv_unpack(p, static_cast<cudaStream_t>(stream));
+}
+
+int pd_kv_unpack(const pd_kv_desc* desc, const pd_batch* batch, const void* src, size_t src_bytes,
+                 const int64_t* src_offsets, void* k_pool, void* v_pool, int32_t* dev_status, void* stream) {
+  if (desc == nullptr) return PD_ERR_INVALID_ARG;
+  return pd_kv_unpack_heads(desc, batch, 0, desc->num_kv_heads, src, src_bytes, src_offsets, k_pool, v_pool,
+                            dev_status, stream);
 }
 
 }  // extern "C"

@@ -52,9 +52,10 @@ __device__ __forceinline__ void warp_copy(const uint4* __restrict__ src, uint4* 
   }
 }
 
-// Unit u of a pack / unpack enumerates (request r, layer, K/V, head h, page k of
-// the request) with k fastest, so consecutive warps touch consecutive bytes of
-// the packed buffer. Page k carries tokens [k*P, min((k+1)*P, kv_len)).
+// Unit u of a pack / unpack enumerates (request r, layer, K/V, head h of the
+// range, page k of the request) with k fastest, so consecutive warps touch
+// consecutive bytes of the packed buffer. Page k carries tokens
+// [k*P, min((k+1)*P, kv_len)); packed head h is pool head head_begin + h.
 struct Unit {
   int r, layer, kv, h, k;
 };
@@ -142,15 +143,15 @@ __global__ void __launch_bounds__(kCopyThreads) kv_pack_kernel(const KvCopyParam
   const int64_t warp0 = ((int64_t)blockIdx.x * kCopyThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kCopyThreads) >> 5;
   const int kp = (p.max_kv_len + p.page_size - 1) / p.page_size;
-  const int64_t units = (int64_t)p.batch * p.num_layers * 2 * p.hkv * kp;
+  const int64_t units = (int64_t)p.batch * p.num_layers * 2 * p.head_count * kp;
   const int vpr = p.head_dim * p.elem_size / 16;
   for (int64_t u = warp0; u < units; u += nwarps) {
-    const Unit x = unit_of(u, kp, p.hkv, p.num_layers);
+    const Unit x = unit_of(u, kp, p.head_count, p.num_layers);
     const int n = __ldg(p.kv_len + x.r);
     if ((int64_t)x.k * p.page_size >= n) continue;
     const int pa = __ldg(p.page_indptr + x.r), pb = __ldg(p.page_indptr + x.r + 1);
     const int64_t off = __ldg(p.offsets + x.r);
-    const int64_t block = (int64_t)p.num_layers * 2 * p.hkv * n * vpr * 16;
+    const int64_t block = (int64_t)p.num_layers * 2 * p.head_count * n * vpr * 16;
     const bool bad_off = (off & 15) != 0 || off < 0 || off + block > p.buf_bytes;
     if (n > p.max_kv_len || pa < 0 || (int64_t)(pb - pa) * p.page_size < n || bad_off) {
       if (lane == 0) report(p.status, bad_off ? PD_DEV_BAD_OFFSET : PD_DEV_BAD_PAGE_TABLE);
@@ -163,9 +164,10 @@ __global__ void __launch_bounds__(kCopyThreads) kv_pack_kernel(const KvCopyParam
     }
     const int rows = min(p.page_size, n - x.k * p.page_size);
     const uint8_t* pool = static_cast<const uint8_t*>(x.kv ? p.src2 : p.src) + (int64_t)x.layer * p.layer_stride;
-    const uint4* src = reinterpret_cast<const uint4*>(pool) + ((int64_t)page * p.hkv + x.h) * p.page_size * vpr;
+    const uint4* src =
+        reinterpret_cast<const uint4*>(pool) + ((int64_t)page * p.hkv + p.head_begin + x.h) * p.page_size * vpr;
     uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dst) + off) +
-                 ((((int64_t)x.layer * 2 + x.kv) * p.hkv + x.h) * n + (int64_t)x.k * p.page_size) * vpr;
+                 ((((int64_t)x.layer * 2 + x.kv) * p.head_count + x.h) * n + (int64_t)x.k * p.page_size) * vpr;
     warp_copy(src, dst, rows * vpr, lane);
   }
 }
@@ -176,15 +178,15 @@ __global__ void __launch_bounds__(kCopyThreads) kv_unpack_kernel(const KvCopyPar
   const int64_t warp0 = ((int64_t)blockIdx.x * kCopyThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kCopyThreads) >> 5;
   const int kp = (p.max_kv_len + p.page_size - 1) / p.page_size;
-  const int64_t units = (int64_t)p.batch * p.num_layers * 2 * p.hkv * kp;
+  const int64_t units = (int64_t)p.batch * p.num_layers * 2 * p.head_count * kp;
   const int vpr = p.head_dim * p.elem_size / 16;
   for (int64_t u = warp0; u < units; u += nwarps) {
-    const Unit x = unit_of(u, kp, p.hkv, p.num_layers);
+    const Unit x = unit_of(u, kp, p.head_count, p.num_layers);
     const int n = __ldg(p.kv_len + x.r);
     if ((int64_t)x.k * p.page_size >= n) continue;
     const int pa = __ldg(p.page_indptr + x.r), pb = __ldg(p.page_indptr + x.r + 1);
     const int64_t off = __ldg(p.offsets + x.r);
-    const int64_t block = (int64_t)p.num_layers * 2 * p.hkv * n * vpr * 16;
+    const int64_t block = (int64_t)p.num_layers * 2 * p.head_count * n * vpr * 16;
     const bool bad_off = (off & 15) != 0 || off < 0 || off + block > p.buf_bytes;
     if (n > p.max_kv_len || pa < 0 || (int64_t)(pb - pa) * p.page_size < n || bad_off) {
       if (lane == 0) report(p.status, bad_off ? PD_DEV_BAD_OFFSET : PD_DEV_BAD_PAGE_TABLE);
@@ -197,9 +199,9 @@ __global__ void __launch_bounds__(kCopyThreads) kv_unpack_kernel(const KvCopyPar
     }
     const int rows = min(p.page_size, n - x.k * p.page_size);
     uint8_t* pool = static_cast<uint8_t*>(x.kv ? p.dst2 : p.dst) + (int64_t)x.layer * p.layer_stride;
-    uint4* dst = reinterpret_cast<uint4*>(pool) + ((int64_t)page * p.hkv + x.h) * p.page_size * vpr;
+    uint4* dst = reinterpret_cast<uint4*>(pool) + ((int64_t)page * p.hkv + p.head_begin + x.h) * p.page_size * vpr;
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.src) + off) +
-                       ((((int64_t)x.layer * 2 + x.kv) * p.hkv + x.h) * n + (int64_t)x.k * p.page_size) * vpr;
+                       ((((int64_t)x.layer * 2 + x.kv) * p.head_count + x.h) * n + (int64_t)x.k * p.page_size) * vpr;
     warp_copy(src, dst, rows * vpr, lane);
   }
 }

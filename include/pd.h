@@ -248,6 +248,28 @@ PD_API int pd_kv_unpack(const pd_kv_desc *desc, const pd_batch *batch, const voi
                         int32_t *dev_status, void *stream);
 
 /*
+ * Head-range forms of pack and unpack (section "Sharded KV cache transfers":
+ * when prefiller and decoder shard the KV heads differently, pages are split or
+ * rebuilt by the ratio of the slices). desc->num_kv_heads is the pool's head
+ * count; the call moves pool heads [head_begin, head_begin + head_count), and
+ * each request's block holds those heads only:
+ * [L][2 (K, V)][head_count][kv_len[r]][D]. Example: two prefiller shards with
+ * 20 heads each pack their own pools; the decoder unpacks the two blocks into
+ * one 40-head pool with head_begin 0 and 20. pd_kv_pack / pd_kv_unpack are the
+ * full range. head_begin < 0, head_count < 1 or a range past the pool's heads
+ * return PD_ERR_INVALID_ARG. Other arguments, checks and errors as pd_kv_pack /
+ * pd_kv_unpack.
+ */
+PD_API int pd_kv_pack_heads(const pd_kv_desc *desc, const pd_batch *batch, int32_t head_begin,
+                            int32_t head_count, const void *k_pool, const void *v_pool, void *dst,
+                            size_t dst_bytes, const int64_t *dst_offsets, int32_t *dev_status,
+                            void *stream);
+PD_API int pd_kv_unpack_heads(const pd_kv_desc *desc, const pd_batch *batch, int32_t head_begin,
+                              int32_t head_count, const void *src, size_t src_bytes,
+                              const int64_t *src_offsets, void *k_pool, void *v_pool,
+                              int32_t *dev_status, void *stream);
+
+/*
  * Profiling hook (not part of the method): while set, every call of this host
  * thread records `start_event` on its stream just before launching its main
  * kernel (the split-KV decode kernel, the prefill/mixed kernel, the append,

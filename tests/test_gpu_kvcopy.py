@@ -137,3 +137,41 @@ def test_pack_bad_offset_is_reported():
                   dev_tensor(hc.src_table.page_indices), buf, offs, max_kv_len=16, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 6
+
+
+def test_sharded_handoff_tp2_to_tp1_and_back():
+    # two prefiller shards hold kv heads [0, 4) and [4, 8); each packs its own
+    # pool and the decoder (all 8 heads, page 64) unpacks both blocks at head
+    # offsets 0 and 4; then head ranges of the decoder pool are packed again
+    hc = wl.kv_handoff(seed=206, batch=3, layers=3, heads=8, head_dim=128, src_page=16, dst_page=64,
+                       dtype=wl.BF16, kv_lens=[100, 17, 64], src_slack=3, dst_slack=2)
+    L, H, D, half = 3, 8, 128, 4
+    kv_len = dev_tensor(hc.kv_len.astype(np.int32))
+    s_ptr, s_idx = dev_tensor(hc.src_table.page_indptr), dev_tensor(hc.src_table.page_indices)
+    d_ptr, d_idx = dev_tensor(hc.dst_table.page_indptr), dev_tensor(hc.dst_table.page_indices)
+    half_bytes = wl.packed_bytes(hc.kv_len, L, half, D, 2)
+    half_offs_h = (hc.dst_offsets // 2).astype(np.int64)
+    half_offs = dev_tensor(half_offs_h)
+    shape = (L, hc.dst_table.num_pages, H, 64, D)
+    k1, v1 = dev_tensor(wl._poison(shape, hc.dtype)), dev_tensor(wl._poison(shape, hc.dtype))
+    for s in range(2):
+        ks = dev_tensor(np.ascontiguousarray(hc.k_src[:, :, s * half:(s + 1) * half]))
+        vs = dev_tensor(np.ascontiguousarray(hc.v_src[:, :, s * half:(s + 1) * half]))
+        buf = torch.empty(half_bytes, dtype=torch.uint8, device="cuda")
+        pd.pd_kv_pack(ks, vs, kv_len, s_ptr, s_idx, buf, half_offs, max_kv_len=100)
+        pd.pd_kv_unpack_heads(buf, half_offs, k1, v1, kv_len, d_ptr, d_idx, s * half, half, max_kv_len=100)
+    whole = oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, hc.k_src, hc.v_src,
+                           hc.dst_offsets, wl.packed_bytes(hc.kv_len, L, H, D, 2))
+    k_ref, v_ref = wl._poison(shape, hc.dtype), wl._poison(shape, hc.dtype)
+    oracle.kv_unpack(hc.kv_len, hc.dst_table.page_indptr, hc.dst_table.page_indices, whole, hc.dst_offsets,
+                     k_ref, v_ref)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(_bits(k1), _host_bits(k_ref))
+    np.testing.assert_array_equal(_bits(v1), _host_bits(v_ref))
+    for s in range(2):
+        buf = torch.empty(half_bytes, dtype=torch.uint8, device="cuda")
+        pd.pd_kv_pack_heads(k1, v1, kv_len, d_ptr, d_idx, buf, half_offs, s * half, half, max_kv_len=100)
+        ref = oracle.kv_pack(hc.kv_len, hc.dst_table.page_indptr, hc.dst_table.page_indices, k_ref, v_ref,
+                             half_offs_h, half_bytes, head_begin=s * half, head_count=half)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(buf.cpu().numpy(), ref)

@@ -103,3 +103,13 @@ def test_kv_copies_reject_bad_descriptor(lib):
     two_layers = pd.KvDesc(2, 128, 16, pd.PD_BF16, 0, 2, 1 << 20)
     assert lib.pd_kv_append(ctypes.byref(two_layers), ctypes.byref(b), 16, 16, 16, 16, None, None) == \
         pd.PD_ERR_INVALID_ARG
+
+
+def test_head_ranges_outside_the_pool_are_rejected(lib):
+    b = _batch()
+    d = pd.KvDesc(4, 128, 16, pd.PD_BF16, 0, 1, 0)
+    for h0, n in [(-1, 2), (0, 0), (3, 2), (4, 1)]:
+        assert lib.pd_kv_pack_heads(ctypes.byref(d), ctypes.byref(b), h0, n, 16, 16, 16, 1 << 20, 16, None,
+                                    None) == pd.PD_ERR_INVALID_ARG
+        assert lib.pd_kv_unpack_heads(ctypes.byref(d), ctypes.byref(b), h0, n, 16, 1 << 20, 16, 16, 16, None,
+                                      None) == pd.PD_ERR_INVALID_ARG
