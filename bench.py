@@ -52,22 +52,29 @@ def measured_peaks() -> dict:
     return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
-def csrc_hash() -> str:
+# sources each profiled kernel is built from
+KERNEL_SOURCES = {
+    "decode_kernel": ["decode_ragged_paged_gb300/csrc/pd_decode.cu", "decode_ragged_paged_gb300/csrc/pd_common.cuh",
+                      "decode_ragged_paged_gb300/csrc/pd_internal.h", "include/pd.h"],
+}
+
+
+def csrc_hash(kernel: str = "decode_kernel") -> str:
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "decode_ragged_paged_gb300", "csrc", "*"))):
-        h.update(open(f, "rb").read())
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel sources changed since the counters were taken."""
+    kernel's sources changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
         return None
     d = json.load(open(path))
     e = d.get(kernel)
-    if not e or e.get("csrc") != csrc_hash():
+    if not e or e.get("csrc") != csrc_hash(kernel):
         return None
     return e.get("bytes_per_launch")
 
