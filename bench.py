@@ -310,6 +310,75 @@ def timed(fn, reps, warm, flush=None, prof=True):
     return float(np.median(tot)), float(np.median(ker)), float(np.median(host)) * 1e6
 
 
+def layer_streamed_row(w, reps: int = 3) -> dict:
+    """The handoff's tail: a model stream appends each of the 40 layers (8 x 512
+    new tokens, 40 heads) and signals a counter; the messenger packs each layer
+    as soon as it is signalled, on its own stream. Compared with packing all
+    layers after the last append: the time from the end of the last append to
+    the last packed byte, and the whole run."""
+    import torch
+    import decode_ragged_paged_gb300 as pd
+    L = w["layers"]
+    n_tok = int(w["kv_len_host"].sum())
+    g = torch.Generator(device=w["k_src"].device)
+    g.manual_seed(11)
+    k_new = torch.randn((n_tok, w["heads"], w["head_dim"]), generator=g, device=w["k_src"].device,
+                        dtype=torch.bfloat16)
+    v_new = torch.randn_like(k_new)
+    new_indptr = torch.zeros(len(w["kv_len_host"]) + 1, dtype=torch.int32, device=k_new.device)
+    new_indptr[1:] = torch.cumsum(w["kv_len"], 0)
+    model, msg = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def appends(stream, signal=None):
+        with torch.cuda.stream(stream):
+            for layer in range(L):
+                pd.pd_kv_append(k_new, v_new, w["k_src"][layer], w["v_src"][layer], new_indptr, w["kv_len"],
+                                w["src_indptr"], w["src_indices"], max_kv_len=512, stream=stream)
+                if signal is not None:
+                    pd.pd_layer_signal(signal, layer + 1, stream=stream)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    serial, streamed = [], []
+    host_w, dev_w = pd.pd_counter_alloc()
+    try:
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            a, b, c = ev(), ev(), ev()
+            a.record(model)
+            appends(model)
+            b.record(model)
+            pd.pd_kv_pack(w["k_src"], w["v_src"], w["kv_len"], w["src_indptr"], w["src_indices"], w["buffer"],
+                          w["offsets"], max_kv_len=512, stream=model)
+            c.record(model)
+            torch.cuda.synchronize()
+            serial.append((b.elapsed_time(c), a.elapsed_time(c)))
+
+            ctypes_u32 = __import__("ctypes").c_uint32.from_address(host_w)
+            ctypes_u32.value = 0
+            torch.cuda.synchronize()
+            a, b, c = ev(), ev(), ev()
+            a.record(model)
+            h = pd.pd_messenger_start_pack(host_w, w["k_src"], w["v_src"], w["kv_len"], w["src_indptr"],
+                                           w["src_indices"], w["buffer"], w["offsets"], timeout_ms=5000,
+                                           max_kv_len=512, stream=msg)
+            appends(model, signal=dev_w)
+            b.record(model)
+            pd.pd_messenger_join(h)
+            c.record(msg)
+            torch.cuda.synchronize()
+            streamed.append((b.elapsed_time(c), a.elapsed_time(c)))
+    finally:
+        torch.cuda.synchronize()
+        pd.pd_counter_free(host_w)
+    med = lambda xs, i: round(float(np.median([x[i] for x in xs])), 4)
+    return {"workload": "40 layers: append of 8 x 512 new tokens (40 kv heads, D 128, bf16) then pack per layer",
+            "tail_streamed_ms": med(streamed, 0), "tail_after_all_layers_ms": med(serial, 0),
+            "total_streamed_ms": med(streamed, 1), "total_serial_ms": med(serial, 1),
+            "note": "tail = end of the last append to the last packed byte"}
+
+
 def measure_rows(args, dev, peaks) -> dict:
     """The other steps of the hot path, each on its own workload."""
     import torch
@@ -418,6 +487,8 @@ def measure_rows(args, dev, peaks) -> dict:
                       "kernel_ms": round(kms, 5), "host_us": round(hus, 1),
                       "GBs": round(byts / kms / 1e6, 1), "frac_hbm": round(byts / kms / 1e6 / hbm, 4),
                       "bound": "hbm", "bytes": byts}
+    rows["layer_streamed_handoff"] = layer_streamed_row(w, reps=3)
+
     # sharded handoff (TP2 prefiller -> TP1 decoder): two blocks of 20 heads
     # unpacked into heads [0, 20) and [20, 40) of one 40-head pool
     half = w["buffer"][: w["buffer"].numel() // 2]

@@ -25,7 +25,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpd.so")
 
-PD_OK, PD_ERR_INVALID_ARG, PD_ERR_UNSUPPORTED, PD_ERR_WORKSPACE, PD_ERR_CUDA = 0, -1, -2, -3, -4
+PD_OK, PD_ERR_INVALID_ARG, PD_ERR_UNSUPPORTED, PD_ERR_WORKSPACE, PD_ERR_CUDA, PD_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 PD_F32, PD_BF16 = 0, 1
 PD_LAYOUT_HND = 0
 PD_KIND_DECODE, PD_KIND_PREFILL, PD_KIND_MIXED = 0, 1, 2
@@ -36,12 +36,16 @@ DEVICE_STATUS = {0: "ok", 1: "bad indptr", 2: "bad length", 3: "bad page table",
 EXPORTS = ("pd_attn_workspace_size", "pd_attn_decode", "pd_attn_decode_static", "pd_attn_prefill",
            "pd_attn_mixed",
            "pd_kv_append", "pd_kv_pack", "pd_kv_unpack", "pd_kv_pack_heads", "pd_kv_unpack_heads",
+           "pd_kv_pack_layers", "pd_counter_alloc", "pd_counter_free", "pd_layer_signal",
+           "pd_messenger_start_pack", "pd_messenger_join",
            "pd_profile_events", "pd_status_string",
            "pd_device_status_string", "pd_version")
 
 
 class PdError(RuntimeError):
-    pass
+    def __init__(self, msg: str, code: int = 0):
+        super().__init__(msg)
+        self.code = code
 
 
 class AttnDesc(ctypes.Structure):
@@ -91,7 +95,19 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                              P, P]
             lib.pd_kv_unpack_heads.argtypes = [ctypes.POINTER(KvDesc), ctypes.POINTER(Batch), I32, I32, P, S, P, P,
                                                P, P, P]
-            for name in ("pd_kv_append", "pd_kv_pack", "pd_kv_unpack", "pd_kv_pack_heads", "pd_kv_unpack_heads"):
+            lib.pd_kv_pack_layers.argtypes = lib.pd_kv_pack_heads.argtypes
+            for name in ("pd_kv_append", "pd_kv_pack", "pd_kv_unpack", "pd_kv_pack_heads", "pd_kv_unpack_heads",
+                         "pd_kv_pack_layers"):
+                getattr(lib, name).restype = ctypes.c_int
+            PP = ctypes.POINTER(ctypes.c_void_p)
+            lib.pd_counter_alloc.argtypes = [PP, PP]
+            lib.pd_counter_free.argtypes = [P]
+            lib.pd_layer_signal.argtypes = [P, ctypes.c_uint32, P]
+            lib.pd_messenger_start_pack.argtypes = [PP, P, ctypes.POINTER(KvDesc), ctypes.POINTER(Batch), P, P, P,
+                                                    S, P, P, P, I32]
+            lib.pd_messenger_join.argtypes = [P, ctypes.POINTER(I32)]
+            for name in ("pd_counter_alloc", "pd_counter_free", "pd_layer_signal", "pd_messenger_start_pack",
+                         "pd_messenger_join"):
                 getattr(lib, name).restype = ctypes.c_int
             lib.pd_status_string.argtypes = [I32]
             lib.pd_status_string.restype = ctypes.c_char_p
@@ -107,7 +123,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 def _check(rc: int, what: str) -> None:
     if rc != PD_OK:
         msg = load_library().pd_status_string(rc).decode()
-        raise PdError(f"{what} failed: {msg} ({rc})")
+        raise PdError(f"{what} failed: {msg} ({rc})", rc)
 
 
 def _ptr(t) -> int | None:
@@ -286,6 +302,65 @@ def pd_kv_unpack_heads(src, src_offsets, k_pools, v_pools, kv_len, page_indptr, 
                                 _ptr(src), src.numel() * src.element_size(), _ptr(src_offsets), _ptr(k_pools),
                                 _ptr(v_pools), _ptr(dev_status), _stream(stream))
     _check(rc, "pd_kv_unpack_heads")
+
+
+def pd_kv_pack_layers(k_pools, v_pools, kv_len, page_indptr, page_indices, dst, dst_offsets, layer_begin,
+                      layer_count, *, max_kv_len=None, dev_status=None, stream=None):
+    """pd_kv_pack of layers [layer_begin, layer_begin + layer_count) into their places of the full blocks."""
+    lib = load_library()
+    L, stride, num_pages = _layers(k_pools)
+    desc = _kv_desc(k_pools, L, stride)
+    batch = make_batch(kv_len, page_indptr, page_indices, num_pages, max_kv_len=max_kv_len)
+    rc = lib.pd_kv_pack_layers(ctypes.byref(desc), ctypes.byref(batch), int(layer_begin), int(layer_count),
+                               _ptr(k_pools), _ptr(v_pools), _ptr(dst), dst.numel() * dst.element_size(),
+                               _ptr(dst_offsets), _ptr(dev_status), _stream(stream))
+    _check(rc, "pd_kv_pack_layers")
+
+
+def pd_counter_alloc():
+    """One mapped pinned 32-bit word set to 0: returns (host address, device address)."""
+    h, d = ctypes.c_void_p(), ctypes.c_void_p()
+    _check(load_library().pd_counter_alloc(ctypes.byref(h), ctypes.byref(d)), "pd_counter_alloc")
+    return h.value, d.value
+
+
+def pd_counter_free(host_word) -> None:
+    _check(load_library().pd_counter_free(host_word), "pd_counter_free")
+
+
+def counter_value(host_word) -> int:
+    """Current value of a counter from pd_counter_alloc (read on the host)."""
+    return ctypes.c_uint32.from_address(host_word).value
+
+
+def pd_layer_signal(device_word, value: int, stream=None) -> None:
+    """Enqueue the write of `value` to the counter once earlier work on the stream has completed."""
+    _check(load_library().pd_layer_signal(device_word, int(value), _stream(stream)), "pd_layer_signal")
+
+
+def pd_messenger_start_pack(host_word, k_pools, v_pools, kv_len, page_indptr, page_indices, dst, dst_offsets, *,
+                            timeout_ms=1000, max_kv_len=None, dev_status=None, stream=None):
+    """Start the host thread that packs each layer once the counter passes it; returns its handle."""
+    lib = load_library()
+    L, stride, num_pages = _layers(k_pools)
+    desc = _kv_desc(k_pools, L, stride)
+    batch = make_batch(kv_len, page_indptr, page_indices, num_pages, max_kv_len=max_kv_len)
+    handle = ctypes.c_void_p()
+    rc = lib.pd_messenger_start_pack(ctypes.byref(handle), host_word, ctypes.byref(desc), ctypes.byref(batch),
+                                     _ptr(k_pools), _ptr(v_pools), _ptr(dst), dst.numel() * dst.element_size(),
+                                     _ptr(dst_offsets), _ptr(dev_status), _stream(stream), int(timeout_ms))
+    _check(rc, "pd_messenger_start_pack")
+    return handle.value
+
+
+def pd_messenger_join(handle) -> int:
+    """Wait for the messenger thread; returns the number of layers enqueued, raises PdError on failure."""
+    sent = ctypes.c_int32(0)
+    rc = load_library().pd_messenger_join(handle, ctypes.byref(sent))
+    if rc != PD_OK:
+        msg = load_library().pd_status_string(rc).decode()
+        raise PdError(f"pd_messenger_join: {msg} ({rc}) after {sent.value} layers", rc)
+    return sent.value
 
 
 def pd_profile_events(start=None, stop=None) -> None:

@@ -87,6 +87,7 @@ const char* pd_status_string(int32_t code) {
     case PD_ERR_UNSUPPORTED: return "unsupported configuration";
     case PD_ERR_WORKSPACE: return "workspace too small";
     case PD_ERR_CUDA: return "CUDA error";
+    case PD_ERR_TIMEOUT: return "timed out waiting for a layer signal";
     default: return "unknown status";
   }
 }
@@ -242,6 +243,8 @@ KvCopyParams kv_params(const pd_kv_desc* d, const pd_batch* b, int32_t* status) 
   p.elem_size = elem_size(d->dtype);
   p.head_begin = 0;
   p.head_count = d->num_kv_heads;
+  p.layer_begin = 0;
+  p.layer_count = d->num_layers;
   p.max_kv_len = b->max_kv_len;
   p.max_new = b->total_qo;
   p.layer_stride = d->layer_stride_bytes;
@@ -284,6 +287,26 @@ int pd_kv_pack_heads(const pd_kv_desc* desc, const pd_batch* batch, int32_t head
   KvCopyParams p = kv_params(desc, batch, dev_status);
   p.head_begin = head_begin;
   p.head_count = head_count;
+  p.src = k_pool;
+  p.src2 = v_pool;
+  p.dst = dst;
+  p.offsets = dst_offsets;
+  p.buf_bytes = (int64_t)dst_bytes;
+  return launch_kv_pack(p, static_cast<cudaStream_t>(stream));
+}
+
+int pd_kv_pack_layers(const pd_kv_desc* desc, const pd_batch* batch, int32_t layer_begin, int32_t layer_count,
+                      const void* k_pool, const void* v_pool, void* dst, size_t dst_bytes,
+                      const int64_t* dst_offsets, int32_t* dev_status, void* stream) {
+  int rc = check_kv(desc, batch);
+  if (rc != PD_OK) return rc;
+  if (layer_begin < 0 || layer_count < 1 || layer_count > desc->num_layers - layer_begin) return PD_ERR_INVALID_ARG;
+  if (batch->batch_size == 0) return PD_OK;
+  if (k_pool == nullptr || v_pool == nullptr || dst == nullptr || dst_offsets == nullptr) return PD_ERR_INVALID_ARG;
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(dst)) return PD_ERR_INVALID_ARG;
+  KvCopyParams p = kv_params(desc, batch, dev_status);
+  p.layer_begin = layer_begin;
+  p.layer_count = layer_count;
   p.src = k_pool;
   p.src2 = v_pool;
   p.dst = dst;

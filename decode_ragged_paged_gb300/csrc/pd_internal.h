@@ -94,7 +94,8 @@ int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const vo
 // --------------------------------------------------------------- KV copies
 struct KvCopyParams {
   int32_t batch, hkv, head_dim, page_size, num_layers, num_pages, elem_size;
-  int32_t head_begin, head_count;  // pack / unpack: pool heads [head_begin, head_begin + head_count)
+  int32_t head_begin, head_count;    // pack / unpack: pool heads [head_begin, head_begin + head_count)
+  int32_t layer_begin, layer_count;  // pack: layers [layer_begin, layer_begin + layer_count) of num_layers
   int32_t max_kv_len, max_new;
   int64_t layer_stride;
   const int32_t* new_indptr;   // append only

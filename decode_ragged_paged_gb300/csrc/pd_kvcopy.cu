@@ -143,10 +143,11 @@ __global__ void __launch_bounds__(kCopyThreads) kv_pack_kernel(const KvCopyParam
   const int64_t warp0 = ((int64_t)blockIdx.x * kCopyThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kCopyThreads) >> 5;
   const int kp = (p.max_kv_len + p.page_size - 1) / p.page_size;
-  const int64_t units = (int64_t)p.batch * p.num_layers * 2 * p.head_count * kp;
+  const int64_t units = (int64_t)p.batch * p.layer_count * 2 * p.head_count * kp;
   const int vpr = p.head_dim * p.elem_size / 16;
   for (int64_t u = warp0; u < units; u += nwarps) {
-    const Unit x = unit_of(u, kp, p.head_count, p.num_layers);
+    Unit x = unit_of(u, kp, p.head_count, p.layer_count);
+    x.layer += p.layer_begin;  // blocks keep all num_layers layers
     const int n = __ldg(p.kv_len + x.r);
     if ((int64_t)x.k * p.page_size >= n) continue;
     const int pa = __ldg(p.page_indptr + x.r), pb = __ldg(p.page_indptr + x.r + 1);

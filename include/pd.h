@@ -78,7 +78,8 @@ typedef enum {
   PD_ERR_INVALID_ARG = -1, /* null pointer, negative or inconsistent host-side size */
   PD_ERR_UNSUPPORTED = -2, /* valid request this build does not implement */
   PD_ERR_WORKSPACE = -3,   /* workspace smaller than pd_attn_workspace_size() */
-  PD_ERR_CUDA = -4         /* a CUDA runtime call or kernel launch failed */
+  PD_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed */
+  PD_ERR_TIMEOUT = -5      /* a host-side wait (the layer messenger) ran out */
 } pd_status;
 
 /* Codes stored into *dev_status by the kernels (first failure wins). */
@@ -268,6 +269,57 @@ PD_API int pd_kv_unpack_heads(const pd_kv_desc *desc, const pd_batch *batch, int
                               int32_t head_count, const void *src, size_t src_bytes,
                               const int64_t *src_offsets, void *k_pool, void *v_pool,
                               int32_t *dev_status, void *stream);
+
+/*
+ * Layer range of pd_kv_pack (section "KV Messenger": a layer's page copies
+ * start as soon as the model has appended that layer's KV entries). Packs
+ * layers [layer_begin, layer_begin + layer_count) of every request into the
+ * same places of its [L][2][Hkv][kv_len][D] block as the full pack would, with
+ * L = desc->num_layers; k_pool / v_pool point at layer 0's pools. A range
+ * outside [0, L) returns PD_ERR_INVALID_ARG; otherwise as pd_kv_pack.
+ */
+PD_API int pd_kv_pack_layers(const pd_kv_desc *desc, const pd_batch *batch, int32_t layer_begin,
+                             int32_t layer_count, const void *k_pool, const void *v_pool, void *dst,
+                             size_t dst_bytes, const int64_t *dst_offsets, int32_t *dev_status,
+                             void *stream);
+
+/*
+ * Layer-streamed handoff (section "KV Messenger": a polling thread watches a
+ * counter that the GPU advances after each layer; the step stays capturable in
+ * a CUDA graph).
+ *
+ * pd_counter_alloc: one 32-bit word of mapped pinned host memory, set to 0;
+ * host_word is its host address, device_word the address kernels write. Freed
+ * by pd_counter_free(host_word).
+ *
+ * pd_layer_signal: enqueues on `stream` a one-thread kernel that stores
+ * `value` to device_word with a system-scope release store once every earlier
+ * kernel on the stream has completed. A model signals value l + 1 after
+ * appending layer l. The call is a kernel launch, so it can be captured.
+ *
+ * pd_messenger_start_pack: starts a host thread that, for each layer l of
+ * desc->num_layers in order, waits until *host_word > l (at most timeout_ms,
+ * counted from when it starts waiting for that layer), then enqueues
+ * pd_kv_pack_layers(l, 1) with the given arguments on `stream` (the
+ * messenger's own stream; the caller's model runs on another). Descriptor
+ * structs are copied; buffers must stay alive until the packs have run.
+ * Returns PD_OK and the handle in *out, or PD_ERR_INVALID_ARG (null
+ * arguments, timeout_ms <= 0) and nothing started.
+ *
+ * pd_messenger_join: waits for the thread and frees the handle. Returns PD_OK
+ * when every layer's pack was enqueued; PD_ERR_TIMEOUT when a layer's signal
+ * did not arrive in time; or the error of a failed pd_kv_pack_layers. Layers
+ * enqueued before the failure are reported in *layers_sent (may be NULL).
+ */
+typedef struct pd_messenger pd_messenger;
+PD_API int pd_counter_alloc(uint32_t **host_word, uint32_t **device_word);
+PD_API int pd_counter_free(uint32_t *host_word);
+PD_API int pd_layer_signal(uint32_t *device_word, uint32_t value, void *stream);
+PD_API int pd_messenger_start_pack(pd_messenger **out, const uint32_t *host_word, const pd_kv_desc *desc,
+                                   const pd_batch *batch, const void *k_pool, const void *v_pool,
+                                   void *dst, size_t dst_bytes, const int64_t *dst_offsets,
+                                   int32_t *dev_status, void *stream, int32_t timeout_ms);
+PD_API int pd_messenger_join(pd_messenger *m, int32_t *layers_sent);
 
 /*
  * Profiling hook (not part of the method): while set, every call of this host

@@ -113,3 +113,54 @@ def test_head_ranges_outside_the_pool_are_rejected(lib):
                                     None) == pd.PD_ERR_INVALID_ARG
         assert lib.pd_kv_unpack_heads(ctypes.byref(d), ctypes.byref(b), h0, n, 16, 1 << 20, 16, 16, 16, None,
                                       None) == pd.PD_ERR_INVALID_ARG
+
+
+def _start(lib, word, batch, timeout_ms):
+    d = pd.KvDesc(2, 128, 16, pd.PD_BF16, 0, 3, 1 << 20)
+    h = ctypes.c_void_p()
+    rc = lib.pd_messenger_start_pack(ctypes.byref(h), ctypes.addressof(word), ctypes.byref(d), ctypes.byref(batch),
+                                     0x1000, 0x1000, 0x1000, 1 << 20, 0x1000, None, None, timeout_ms)
+    return rc, h
+
+
+def test_messenger_times_out_when_no_layer_is_signalled(lib):
+    # host-side failure detection: the counter never advances, the thread gives
+    # up after its timeout and reports it; nothing is launched
+    import time
+    word = ctypes.c_uint32(0)
+    rc, h = _start(lib, word, _batch(), 50)
+    assert rc == pd.PD_OK
+    t0 = time.monotonic()
+    sent = ctypes.c_int32(-1)
+    assert lib.pd_messenger_join(h, ctypes.byref(sent)) == pd.PD_ERR_TIMEOUT
+    assert sent.value == 0 and time.monotonic() - t0 < 5.0
+
+
+def test_messenger_reports_a_failed_layer_pack(lib):
+    # the counter says layer 0 is ready; its pack fails host validation
+    # (no pages), so the thread stops with that error before any launch
+    word = ctypes.c_uint32(1)
+    rc, h = _start(lib, word, _batch(num_pages=0), 1000)
+    assert rc == pd.PD_OK
+    sent = ctypes.c_int32(-1)
+    assert lib.pd_messenger_join(h, ctypes.byref(sent)) == pd.PD_ERR_INVALID_ARG
+    assert sent.value == 0
+
+
+def test_messenger_rejects_bad_arguments(lib):
+    word = ctypes.c_uint32(0)
+    assert _start(lib, word, _batch(), 0)[0] == pd.PD_ERR_INVALID_ARG
+    d = pd.KvDesc(2, 128, 16, pd.PD_BF16, 0, 3, 1 << 20)
+    h = ctypes.c_void_p()
+    assert lib.pd_messenger_start_pack(ctypes.byref(h), None, ctypes.byref(d), ctypes.byref(_batch()), 0x1000, 0x1000,
+                                       0x1000, 1 << 20, 0x1000, None, None, 100) == pd.PD_ERR_INVALID_ARG
+    assert lib.pd_messenger_join(None, None) == pd.PD_ERR_INVALID_ARG
+    assert lib.pd_layer_signal(None, 1, None) == pd.PD_ERR_INVALID_ARG
+
+
+def test_layer_range_outside_the_pool_is_rejected(lib):
+    b = _batch()
+    d = pd.KvDesc(2, 128, 16, pd.PD_BF16, 0, 3, 1 << 20)
+    for l0, n in [(-1, 1), (0, 0), (2, 2), (3, 1)]:
+        assert lib.pd_kv_pack_layers(ctypes.byref(d), ctypes.byref(b), l0, n, 16, 16, 16, 1 << 20, 16, None,
+                                     None) == pd.PD_ERR_INVALID_ARG
