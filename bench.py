@@ -473,6 +473,27 @@ def measure_rows(args, dev, peaks) -> dict:
         rows["mixed"] = {"status": str(e)}
     del w
 
+    # multi-token verification (speculative decoding): the decode batch's shape
+    # with 4 draft tokens per request, bottom-right causal, GQA 32/8 packed
+    # 32 query rows x 4 heads per tensor-core tile
+    rng = np.random.default_rng(1002)
+    kvv = rng.integers(512, 4097, size=128)
+    w = torch_gen.paged_batch(6, [4] * 128, kvv, 32, 8, 128, 16, device=dev)
+    vbytes = int(kvv.sum()) * 8 * 128 * 2 * 2 + 2 * w["q"].numel() * 2
+    try:
+        o = torch.empty_like(w["q"])
+        ms, kms, hus = timed(lambda: pd.pd_attn_mixed(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
+                                                      w["page_indices"], w["qo_indptr"], max_qo_len=4,
+                                                      max_kv_len=4096, o=o), reps, warm, flush)
+        rows["verify_decode"] = {"workload": "128 requests x 4 draft tokens, kv_len U[512,4096], GQA 32/8, D 128, "
+                                             "page 16, bf16 (pd_attn_mixed)",
+                                 "ms": round(ms, 5), "kernel_ms": round(kms, 5), "host_us": round(hus, 1),
+                                 "GBs": round(vbytes / kms / 1e6, 1), "frac_hbm": round(vbytes / kms / 1e6 / hbm, 4),
+                                 "bound": "hbm", "bytes": vbytes}
+    except pd.PdError as e:
+        rows["verify_decode"] = {"status": str(e)}
+    del w
+
     w = torch_gen.kv_handoff(device=dev)
     byts = 2 * w["buffer"].numel()
     ms, kms, hus = timed(lambda: pd.pd_kv_pack(w["k_src"], w["v_src"], w["kv_len"], w["src_indptr"], w["src_indices"],

@@ -109,7 +109,9 @@ size_t pd_attn_workspace_size(const pd_attn_desc* desc, const pd_batch* batch, i
   if (check_attn(desc, batch, false) != PD_OK) return 0;
   if (kind == PD_KIND_DECODE) return decode_layout_for(desc, batch).total;
   if (kind == PD_KIND_PREFILL || kind == PD_KIND_MIXED)
-    return prefill_layout(batch->batch_size, batch->total_qo, batch->max_qo_len).total;
+    return prefill_layout(batch->batch_size, batch->total_qo, batch->max_qo_len,
+                          prefill_tile_heads(desc->num_qo_heads / desc->num_kv_heads))
+        .total;
   return 0;
 }
 
@@ -174,7 +176,8 @@ int pd_attn_prefill(const pd_attn_desc* desc, const pd_batch* batch, const void*
     return PD_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o) || !aligned16(workspace))
     return PD_ERR_INVALID_ARG;
-  const PrefillLayout L = prefill_layout(batch->batch_size, batch->total_qo, batch->max_qo_len);
+  const int32_t tile_heads = prefill_tile_heads(desc->num_qo_heads / desc->num_kv_heads);
+  const PrefillLayout L = prefill_layout(batch->batch_size, batch->total_qo, batch->max_qo_len, tile_heads);
   if (workspace_bytes < L.total) return PD_ERR_WORKSPACE;
   PrefillParams p{};
   p.batch = batch->batch_size;
@@ -189,6 +192,9 @@ int pd_attn_prefill(const pd_attn_desc* desc, const pd_batch* batch, const void*
   p.causal = desc->causal ? 1 : 0;
   p.o_dtype = desc->o_dtype;
   p.max_rq = L.max_rq;
+  p.tile_heads = tile_heads;
+  p.tile_rows = 128 / tile_heads;
+  p.item_heads = p.hq / tile_heads;
   p.scale_log2 = scale_of(desc) * kLog2e;
   p.qo_indptr = batch->qo_indptr;
   p.kv_len = batch->kv_len;

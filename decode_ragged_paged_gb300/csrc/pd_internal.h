@@ -66,6 +66,10 @@ int launch_decode(DecodeParams& p, int32_t kv_dtype, cudaStream_t stream);
 struct PrefillParams {
   int32_t batch, hq, hkv, group, page_size, num_pages, total_qo, max_qo_len, max_kv_len, causal, o_dtype;
   int32_t max_rq;
+  // GQA packing: a 128-row tile holds tile_rows query rows x tile_heads query
+  // heads of one KV head (tile_heads = the group, or 1); items per q tile =
+  // item_heads = hq / tile_heads
+  int32_t tile_heads, tile_rows, item_heads;
   float scale_log2;  // softmax scale times log2(e)
   const int32_t* qo_indptr;
   const int32_t* kv_len;
@@ -83,7 +87,10 @@ struct PrefillLayout {
   int32_t max_rq;
 };
 
-PrefillLayout prefill_layout(int32_t batch, int32_t total_qo, int32_t max_qo_len);
+// Query heads a prefill tile packs for this group size (the group when it
+// divides 128, else 1).
+int32_t prefill_tile_heads(int32_t group);
+PrefillLayout prefill_layout(int32_t batch, int32_t total_qo, int32_t max_qo_len, int32_t tile_heads);
 
 // Checks what the tensor-core prefill supports; returns a pd_status.
 int prefill_supported(int32_t kv_dtype, int32_t head_dim, int32_t page_size);
@@ -119,7 +126,7 @@ int launch_kv_unpack(const KvCopyParams& p, cudaStream_t stream);
 bool make_pool_map(CUtensorMap* map, const void* pool, int32_t dtype, int32_t num_pages, int32_t hkv,
                    int32_t page_size, int32_t head_dim, int32_t box_cols, int32_t box_rows, bool swizzle128);
 bool make_rows_map(CUtensorMap* map, const void* base, int32_t dtype, int32_t total, int32_t hq, int32_t head_dim,
-                   int32_t box_cols, int32_t box_rows, bool swizzle128);
+                   int32_t box_cols, int32_t box_rows, bool swizzle128, int32_t box_heads = 1);
 
 // ------------------------------------------------------------------- misc
 int device_sm_count();

@@ -86,15 +86,18 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
+// An item is (request, q tile of p.tile_rows query rows, group of p.tile_heads
+// query heads sharing KV head g). Tile row m holds query row q0 + m / tile_heads
+// of head h + m % tile_heads (with tile_heads = 1: one head, 128 rows).
 struct PItem {
   int r, qt, h, g, q0, rows, qo_len, kv, n_kv, pbase, need;
 };
 
-__device__ __forceinline__ int kv_tiles(int qt, int qo_len, int kv, int causal) {
+__device__ __forceinline__ int kv_tiles(int qt, int qo_len, int kv, int causal, int tile_rows) {
   if (kv <= 0) return 0;
   int last_key = kv - 1;
   if (causal) {
-    const int last_row = min(qt * kBM + kBM - 1, qo_len - 1);
+    const int last_row = min(qt * tile_rows + tile_rows - 1, qo_len - 1);
     last_key = min(last_key, kv - qo_len + last_row);
   }
   return last_key < 0 ? 0 : last_key / kBN + 1;
@@ -102,18 +105,18 @@ __device__ __forceinline__ int kv_tiles(int qt, int qo_len, int kv, int causal) 
 
 __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int it) {
   PItem I;
-  const int rq = it / p.hq;
-  I.h = it - rq * p.hq;
+  const int rq = it / p.item_heads;
+  I.h = (it - rq * p.item_heads) * p.tile_heads;  // first query head of the tile
   const int2 v = p.rq_list[rq];
   I.r = v.x;
   I.qt = v.y;
   I.g = I.h / p.group;
   const int a = p.qo_indptr[I.r];
   I.qo_len = p.qo_indptr[I.r + 1] - a;
-  I.q0 = a + I.qt * kBM;
-  I.rows = min(kBM, I.qo_len - I.qt * kBM);
+  I.q0 = a + I.qt * p.tile_rows;
+  I.rows = min(p.tile_rows, I.qo_len - I.qt * p.tile_rows);  // valid query rows
   I.kv = p.kv_len[I.r];
-  I.n_kv = kv_tiles(I.qt, I.qo_len, I.kv, p.causal);
+  I.n_kv = kv_tiles(I.qt, I.qo_len, I.kv, p.causal, p.tile_rows);
   I.pbase = p.page_indptr[I.r];
   I.need = (I.kv + p.page_size - 1) / p.page_size;
   return I;
@@ -197,7 +200,8 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
   for (int r = tid; r < p.batch; r += blockDim.x) {
     if (!request_ok(p, r)) continue;
     const int qo = p.qo_indptr[r + 1] - p.qo_indptr[r], n = p.kv_len[r];
-    for (int qt = 0; qt * kBM < qo; ++qt) atomicAdd(&hist[min(kv_tiles(qt, qo, n, p.causal), kBuckets - 1)], 1);
+    for (int qt = 0; qt * p.tile_rows < qo; ++qt)
+      atomicAdd(&hist[min(kv_tiles(qt, qo, n, p.causal, p.tile_rows), kBuckets - 1)], 1);
   }
   __syncthreads();
   {
@@ -225,14 +229,14 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
     }
     __syncthreads();
     cursor[b] = (warp > 0 ? warp_tot[warp - 1] : 0) + x - c;
-    if (tid == 0) p.hdr[0] = min(warp_tot[31], p.max_rq) * p.hq;
+    if (tid == 0) p.hdr[0] = min(warp_tot[31], p.max_rq) * p.item_heads;
   }
   __syncthreads();
   for (int r = tid; r < p.batch; r += blockDim.x) {
     if (!request_ok(p, r)) continue;
     const int qo = p.qo_indptr[r + 1] - p.qo_indptr[r], n = p.kv_len[r];
-    for (int qt = 0; qt * kBM < qo; ++qt) {
-      const int pos = atomicAdd(&cursor[min(kv_tiles(qt, qo, n, p.causal), kBuckets - 1)], 1);
+    for (int qt = 0; qt * p.tile_rows < qo; ++qt) {
+      const int pos = atomicAdd(&cursor[min(kv_tiles(qt, qo, n, p.causal, p.tile_rows), kBuckets - 1)], 1);
       if (pos < p.max_rq) p.rq_list[pos] = make_int2(r, qt);
     }
   }
@@ -443,14 +447,15 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
     // published: the wait for item i's last P V then overlaps useful work.
     // Items alternate between the two O accumulators.
     const int wq = warp & 3;
-    const int row = wq * 32 + lane;
+    const int row = wq * 32 + lane;  // tile row: query row qrow of head (first head) + qhead
+    const int qrow = row / p.tile_heads, qhead = row - qrow * p.tile_heads;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     uint32_t s_ctr = 0, o_phase = 0, it_ctr = 0;
     const bool o_issuer = (warp == 2 && lane == 0);
     int pending_q = -1;  // Q buffer holding an O tile whose TMA store may still read it
     bool ok = true;
     struct Pend {
-      int q0, h, rows, n_kv, qb, ob;
+      int q0, h, rows, n_kv, qb, ob;  // h: the tile's first query head; rows: valid query rows
       uint32_t last;  // running index of the item's last tile
       float m, l;
     };
@@ -472,8 +477,8 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         tc_fence_after();
       }
       const float inv_l = E.l > 0.f ? 1.0f / E.l : 0.f;
-      const bool store = row < E.rows;
-      const int64_t orow = ((int64_t)(E.q0 + row) * p.hq + E.h) * kD;
+      const bool store = qrow < E.rows;
+      const int64_t orow = ((int64_t)(E.q0 + qrow) * p.hq + E.h + qhead) * kD;
       const uint32_t o_addr = t_lane + col_o(E.ob);
       uint32_t v[kD];
       if (E.n_kv > 0) {
@@ -486,7 +491,7 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
 #pragma unroll
         for (int e = 0; e < kD; ++e) v[e] = 0u;
       }
-      const bool staged = p.o_dtype == PD_BF16 && E.rows == kBM;
+      const bool staged = p.o_dtype == PD_BF16 && E.rows == p.tile_rows;
       if (staged) {
         // full tile: stage bf16 O (128-byte swizzled like Q) in the item's Q
         // buffer, free now that its last S product has completed, and write it
@@ -535,7 +540,8 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         }
       }
       if (store && p.lse != nullptr)
-        p.lse[(int64_t)(E.q0 + row) * p.hq + E.h] = (E.n_kv > 0 && E.l > 0.f) ? (E.m + log2f(E.l)) * kLn2 : -INFINITY;
+        p.lse[(int64_t)(E.q0 + qrow) * p.hq + E.h + qhead] =
+            (E.n_kv > 0 && E.l > 0.f) ? (E.m + log2f(E.l)) * kLn2 : -INFINITY;
       if (o_issuer && !staged) mbar_arrive(&bars->q_empty[E.qb]);  // nothing staged in this Q buffer
       tc_fence_before();
       return true;
@@ -546,7 +552,7 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       nxt = prefill_item_or_empty(p, it + gridDim.x, n_items);
       const int qb = it_ctr & 1, ob = it_ctr & 1;
       const uint32_t o_addr = t_lane + col_o(ob);
-      const int lim = I.kv - I.qo_len + I.qt * kBM + row;  // last key this row may see (causal)
+      const int lim = I.kv - I.qo_len + I.qt * p.tile_rows + qrow;  // last key this row may see (causal)
       // l: sum of the weights (normalises O, gives the lse); P enters P V
       // rounded to bf16, an unbiased rounding far inside the output tolerance
       float m = -INFINITY, l = 0.f;
@@ -679,10 +685,19 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
 }
 
 // ------------------------------------------------------------------- host
-PrefillLayout prefill_layout(int32_t batch, int32_t total_qo, int32_t max_qo_len) {
+// GQA packing on (1) or off (0: one query head per tile, any group).
+#ifndef PD_PREFILL_GQA_PACK
+#define PD_PREFILL_GQA_PACK 1
+#endif
+int32_t prefill_tile_heads(int32_t group) {
+  return PD_PREFILL_GQA_PACK && group >= 1 && kBM % group == 0 ? group : 1;
+}
+
+PrefillLayout prefill_layout(int32_t batch, int32_t total_qo, int32_t max_qo_len, int32_t tile_heads) {
   PrefillLayout L{};
-  const int64_t by_len = (int64_t)batch * ((max_qo_len + kBM - 1) / kBM);
-  const int64_t by_rows = (int64_t)(total_qo + kBM - 1) / kBM + batch;
+  const int rows = kBM / (tile_heads > 0 ? tile_heads : 1);
+  const int64_t by_len = (int64_t)batch * ((max_qo_len + rows - 1) / rows);
+  const int64_t by_rows = (int64_t)(total_qo + rows - 1) / rows + batch;
   L.max_rq = (int32_t)(by_len < by_rows ? by_len : by_rows);
   if (L.max_rq < 1) L.max_rq = 1;
   size_t off = 0;
@@ -705,9 +720,10 @@ int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const vo
   CUtensorMap tq, tk, tv, to;
   const int pb = p.page_size < kBN ? p.page_size : kBN;
   memset(&to, 0, sizeof(to));
-  if (p.o_dtype == PD_BF16 && !make_rows_map(&to, p.o, PD_BF16, p.total_qo, p.hq, kD, 64, kBM, true))
+  if (p.o_dtype == PD_BF16 &&
+      !make_rows_map(&to, p.o, PD_BF16, p.total_qo, p.hq, kD, 64, p.tile_rows, true, p.tile_heads))
     return PD_ERR_CUDA;
-  if (!make_rows_map(&tq, q, PD_BF16, p.total_qo, p.hq, kD, 64, kBM, true) ||
+  if (!make_rows_map(&tq, q, PD_BF16, p.total_qo, p.hq, kD, 64, p.tile_rows, true, p.tile_heads) ||
       !make_pool_map(&tk, k_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true) ||
       !make_pool_map(&tv, v_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true))
     return PD_ERR_CUDA;
@@ -722,7 +738,7 @@ int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const vo
   }
   prefill_plan_kernel<<<1, 1024, 0, stream>>>(p);
   int64_t grid = device_sm_count();
-  const int64_t max_items = (int64_t)p.max_rq * p.hq;
+  const int64_t max_items = (int64_t)p.max_rq * p.item_heads;
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
   // A programmatic dependent of the plan (CTAs set up while it finishes),

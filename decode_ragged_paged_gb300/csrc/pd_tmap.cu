@@ -53,15 +53,16 @@ bool make_pool_map(CUtensorMap* map, const void* pool, int32_t dtype, int32_t nu
 }
 
 // q / o rows [total][hq][head_dim] as a 3-D tensor {head_dim, hq, total}; one box
-// = box_rows consecutive rows of one head, box_cols elements wide.
+// = box_rows consecutive rows of box_heads consecutive heads, box_cols elements
+// wide, laid out (row, head)-major in shared memory.
 bool make_rows_map(CUtensorMap* map, const void* base, int32_t dtype, int32_t total, int32_t hq, int32_t head_dim,
-                   int32_t box_cols, int32_t box_rows, bool swizzle128) {
+                   int32_t box_cols, int32_t box_rows, bool swizzle128, int32_t box_heads) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const int es = dtype == PD_BF16 ? 2 : 4;
   cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)hq, (cuuint64_t)total};
   cuuint64_t strides[2] = {(cuuint64_t)head_dim * es, (cuuint64_t)hq * head_dim * es};
-  cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, (cuuint32_t)box_rows};
+  cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = fn(map, tma_dtype(dtype), 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -69,3 +69,21 @@ def test_mixed_bf16_output():
     e = np.floor(np.log2(np.maximum(np.abs(o_ref), 2.0 ** -126)))
     bound = 1e-2 + 2.0 ** (e - 8)
     assert np.all(np.abs(host_f64(o) - o_ref) <= bound)
+
+
+@pytest.mark.parametrize("qo,kv,hq,hkv", [
+    ([4] * 6, [700, 64, 2049, 513, 4, 1000], 32, 8),            # draft verification, GQA 4: 32 rows x 4 heads a tile
+    ([2, 8, 5, 1], [300, 900, 129, 64], 32, 2),                 # GQA 16: 8 query rows x 16 heads a tile
+    ([3, 7], [40, 500], 6, 2),                                  # group 3 does not divide 128: one head a tile
+])
+def test_multi_token_verification_decode(qo, kv, hq, hkv):
+    # a speculative step verifies qo_len draft tokens per request under the
+    # bottom-right causal mask; GQA groups share each KV tile
+    case = wl.make_attn_case(403 + sum(kv), qo, kv, hq, hkv, 128, 16, wl.BF16, causal=True)
+    _, o, lse = run_mixed(case)
+    check_vs_oracle(case, o, lse)
+    d = DevCase(case)
+    o2, lse2 = pd.pd_attn_prefill(d.q, d.k_pool, d.v_pool, d.kv_len, d.page_indptr, d.page_indices, d.qo_indptr,
+                                  max_qo_len=d.max_qo_len, max_kv_len=d.max_kv_len, o_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, o) and torch.equal(lse2, lse)
