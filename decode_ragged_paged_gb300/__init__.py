@@ -38,7 +38,7 @@ EXPORTS = ("pd_attn_workspace_size", "pd_attn_decode", "pd_attn_decode_static", 
            "pd_kv_append", "pd_kv_pack", "pd_kv_unpack", "pd_kv_pack_heads", "pd_kv_unpack_heads",
            "pd_kv_pack_layers", "pd_counter_alloc", "pd_counter_free", "pd_layer_signal",
            "pd_messenger_start_pack", "pd_messenger_join",
-           "pd_profile_events", "pd_status_string",
+           "pd_profile_events", "pd_last_kernel", "pd_status_string",
            "pd_device_status_string", "pd_version")
 
 
@@ -114,6 +114,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.pd_device_status_string.argtypes = [I32]
             lib.pd_device_status_string.restype = ctypes.c_char_p
             lib.pd_version.restype = I32
+            lib.pd_last_kernel.restype = ctypes.c_char_p
             lib.pd_profile_events.argtypes = [P, P]
             lib.pd_profile_events.restype = ctypes.c_int
             _lib = lib
@@ -361,6 +362,11 @@ def pd_messenger_join(handle) -> int:
         msg = load_library().pd_status_string(rc).decode()
         raise PdError(f"pd_messenger_join: {msg} ({rc}) after {sent.value} layers", rc)
     return sent.value
+
+
+def pd_last_kernel() -> str:
+    """Name of the main kernel the last call of this thread launched."""
+    return load_library().pd_last_kernel().decode()
 
 
 def pd_profile_events(start=None, stop=None) -> None:

@@ -24,6 +24,11 @@ int device_sm_count() {
   return n;
 }
 
+const char*& last_kernel() {
+  static thread_local const char* name = "";
+  return name;
+}
+
 ProfileEvents& profile_events() {
   static thread_local ProfileEvents ev;
   return ev;
@@ -58,6 +63,22 @@ float scale_of(const pd_attn_desc* d) {
   return d->sm_scale > 0.f ? d->sm_scale : 1.0f / sqrtf((float)d->head_dim);
 }
 
+// A large GQA decode batch runs faster on the tensor-core kernel with the
+// query heads of a group packed into one tile (one item per request and KV
+// head reads each KV tile once) than on the split-KV kernel; small batches need
+// the split to use the whole GPU, and MHA gains nothing from packing. The
+// tensor-core path takes decode batches without qo_indptr (row r = request r).
+bool decode_on_tensor_cores(const pd_attn_desc* d, const pd_batch* b) {
+  if (b->qo_indptr != nullptr || d->kv_dtype != PD_BF16) return false;
+  if (prefill_supported(d->kv_dtype, d->head_dim, d->page_size) != PD_OK) return false;
+  if (prefill_tile_heads(d->num_qo_heads / d->num_kv_heads) < 2) return false;
+  return (int64_t)b->batch_size * d->num_kv_heads >= 4LL * device_sm_count();
+}
+
+size_t decode_tc_workspace(const pd_batch* b, const pd_attn_desc* d) {
+  return prefill_layout(b->batch_size, b->total_qo, 1, prefill_tile_heads(d->num_qo_heads / d->num_kv_heads)).total;
+}
+
 DecodeLayout decode_layout_for(const pd_attn_desc* d, const pd_batch* b) {
   const int gs = decode_heads_per_item(d->num_qo_heads / d->num_kv_heads, d->head_dim);
   return decode_layout(b->batch_size, d->num_qo_heads, d->head_dim, b->max_kv_len, d->num_qo_heads / gs,
@@ -65,6 +86,44 @@ DecodeLayout decode_layout_for(const pd_attn_desc* d, const pd_batch* b) {
 }
 
 }  // namespace
+
+// Plans and launches the tensor-core kernel; arguments already validated.
+int run_prefill(const pd_attn_desc* desc, const pd_batch* batch, int32_t max_qo_len, int32_t causal, const void* q,
+                const void* k_pool, const void* v_pool, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                int32_t* dev_status, void* stream) {
+  const int32_t tile_heads = prefill_tile_heads(desc->num_qo_heads / desc->num_kv_heads);
+  const PrefillLayout L = prefill_layout(batch->batch_size, batch->total_qo, max_qo_len, tile_heads);
+  if (workspace_bytes < L.total) return PD_ERR_WORKSPACE;
+  PrefillParams p{};
+  p.batch = batch->batch_size;
+  p.hq = desc->num_qo_heads;
+  p.hkv = desc->num_kv_heads;
+  p.group = p.hq / p.hkv;
+  p.page_size = desc->page_size;
+  p.num_pages = batch->num_pages;
+  p.total_qo = batch->total_qo;
+  p.max_qo_len = max_qo_len;
+  p.max_kv_len = batch->max_kv_len;
+  p.causal = causal ? 1 : 0;
+  p.o_dtype = desc->o_dtype;
+  p.max_rq = L.max_rq;
+  p.tile_heads = tile_heads;
+  p.tile_rows = 128 / tile_heads;
+  p.item_heads = p.hq / tile_heads;
+  p.scale_log2 = scale_of(desc) * kLog2e;
+  p.qo_indptr = batch->qo_indptr;
+  p.kv_len = batch->kv_len;
+  p.page_indptr = batch->page_indptr;
+  p.page_indices = batch->page_indices;
+  p.o = o;
+  p.lse = lse;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
+  p.rq_list = reinterpret_cast<int2*>(ws + L.rq_list);
+  p.status = dev_status;
+  return launch_prefill(p, q, k_pool, v_pool, static_cast<cudaStream_t>(stream));
+}
+
 }  // namespace pd
 
 using namespace pd;
@@ -72,6 +131,8 @@ using namespace pd;
 extern "C" {
 
 int32_t pd_version(void) { return 100; }
+
+const char* pd_last_kernel(void) { return last_kernel(); }
 
 int pd_profile_events(void* start_event, void* stop_event) {
   if ((start_event == nullptr) != (stop_event == nullptr)) return PD_ERR_INVALID_ARG;
@@ -107,7 +168,12 @@ const char* pd_device_status_string(int32_t code) {
 
 size_t pd_attn_workspace_size(const pd_attn_desc* desc, const pd_batch* batch, int32_t kind) {
   if (check_attn(desc, batch, false) != PD_OK) return 0;
-  if (kind == PD_KIND_DECODE) return decode_layout_for(desc, batch).total;
+  if (kind == PD_KIND_DECODE) {
+    const size_t split = decode_layout_for(desc, batch).total;
+    if (!decode_on_tensor_cores(desc, batch)) return split;
+    const size_t tc = decode_tc_workspace(batch, desc);
+    return split > tc ? split : tc;
+  }
   if (kind == PD_KIND_PREFILL || kind == PD_KIND_MIXED)
     return prefill_layout(batch->batch_size, batch->total_qo, batch->max_qo_len,
                           prefill_tile_heads(desc->num_qo_heads / desc->num_kv_heads))
@@ -126,6 +192,12 @@ int pd_attn_decode(const pd_attn_desc* desc, const pd_batch* batch, const void* 
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o) || !aligned16(workspace))
     return PD_ERR_INVALID_ARG;
   if (batch->qo_indptr == nullptr && batch->total_qo < batch->batch_size) return PD_ERR_INVALID_ARG;
+  if (decode_on_tensor_cores(desc, batch)) {
+    // one query row per request at the last position: the bottom-right causal
+    // mask admits every key, so the tile runs unmasked (kv_len 0 gives o = 0)
+    return run_prefill(desc, batch, 1, 0, q, k_pool, v_pool, o, lse, workspace, workspace_bytes, dev_status,
+                       stream);
+  }
   const DecodeLayout L = decode_layout_for(desc, batch);
   if (workspace_bytes < L.total) return PD_ERR_WORKSPACE;
 
@@ -176,37 +248,8 @@ int pd_attn_prefill(const pd_attn_desc* desc, const pd_batch* batch, const void*
     return PD_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o) || !aligned16(workspace))
     return PD_ERR_INVALID_ARG;
-  const int32_t tile_heads = prefill_tile_heads(desc->num_qo_heads / desc->num_kv_heads);
-  const PrefillLayout L = prefill_layout(batch->batch_size, batch->total_qo, batch->max_qo_len, tile_heads);
-  if (workspace_bytes < L.total) return PD_ERR_WORKSPACE;
-  PrefillParams p{};
-  p.batch = batch->batch_size;
-  p.hq = desc->num_qo_heads;
-  p.hkv = desc->num_kv_heads;
-  p.group = p.hq / p.hkv;
-  p.page_size = desc->page_size;
-  p.num_pages = batch->num_pages;
-  p.total_qo = batch->total_qo;
-  p.max_qo_len = batch->max_qo_len;
-  p.max_kv_len = batch->max_kv_len;
-  p.causal = desc->causal ? 1 : 0;
-  p.o_dtype = desc->o_dtype;
-  p.max_rq = L.max_rq;
-  p.tile_heads = tile_heads;
-  p.tile_rows = 128 / tile_heads;
-  p.item_heads = p.hq / tile_heads;
-  p.scale_log2 = scale_of(desc) * kLog2e;
-  p.qo_indptr = batch->qo_indptr;
-  p.kv_len = batch->kv_len;
-  p.page_indptr = batch->page_indptr;
-  p.page_indices = batch->page_indices;
-  p.o = o;
-  p.lse = lse;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
-  p.rq_list = reinterpret_cast<int2*>(ws + L.rq_list);
-  p.status = dev_status;
-  return launch_prefill(p, q, k_pool, v_pool, static_cast<cudaStream_t>(stream));
+  return pd::run_prefill(desc, batch, batch->max_qo_len, desc->causal, q, k_pool, v_pool, o, lse, workspace,
+                         workspace_bytes, dev_status, stream);
 }
 
 int pd_attn_mixed(const pd_attn_desc* desc, const pd_batch* batch, const void* q, const void* k_pool,

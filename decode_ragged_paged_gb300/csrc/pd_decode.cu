@@ -731,6 +731,7 @@ int run_decode(DecodeParams& p, cudaStream_t stream) {
   int64_t grid = (int64_t)device_sm_count() * blocks_per_sm;
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
+  last_kernel() = "decode_kernel";
   // Each kernel is a programmatic dependent of the previous one: its CTAs are
   // placed and set up while the previous kernel drains. When the decode kernel
   // is timed alone (profiling events) it runs without that overlap.

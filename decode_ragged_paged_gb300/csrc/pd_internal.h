@@ -136,6 +136,8 @@ struct ProfileEvents {
   cudaEvent_t start = nullptr, stop = nullptr;
 };
 ProfileEvents& profile_events();
+// Name of the main kernel the last call of this host thread launched.
+const char*& last_kernel();
 inline void profile_begin(cudaStream_t s) {
   if (profile_events().start) cudaEventRecord(profile_events().start, s);
 }

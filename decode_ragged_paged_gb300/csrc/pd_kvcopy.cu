@@ -216,6 +216,7 @@ int launch_kv_append(const KvCopyParams& p, cudaStream_t stream) {
   if (p.max_new <= 0 || p.batch <= 0) return PD_OK;
   int grid = copy_grid();
   if (grid > p.max_new) grid = p.max_new;
+  last_kernel() = "kv_append_kernel";
   profile_begin(stream);
   kv_append_kernel<<<grid, kCopyThreads, 0, stream>>>(p);
   profile_end(stream);
@@ -224,6 +225,7 @@ int launch_kv_append(const KvCopyParams& p, cudaStream_t stream) {
 
 int launch_kv_pack(const KvCopyParams& p, cudaStream_t stream) {
   if (p.batch <= 0 || p.max_kv_len <= 0) return PD_OK;
+  last_kernel() = "kv_pack_kernel";
   profile_begin(stream);
   kv_pack_kernel<<<copy_grid(), kCopyThreads, 0, stream>>>(p);
   profile_end(stream);
@@ -232,6 +234,7 @@ int launch_kv_pack(const KvCopyParams& p, cudaStream_t stream) {
 
 int launch_kv_unpack(const KvCopyParams& p, cudaStream_t stream) {
   if (p.batch <= 0 || p.max_kv_len <= 0) return PD_OK;
+  last_kernel() = "kv_unpack_kernel";
   profile_begin(stream);
   kv_unpack_kernel<<<copy_grid(), kCopyThreads, 0, stream>>>(p);
   profile_end(stream);

@@ -111,8 +111,9 @@ __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int it) {
   I.r = v.x;
   I.qt = v.y;
   I.g = I.h / p.group;
-  const int a = p.qo_indptr[I.r];
-  I.qo_len = p.qo_indptr[I.r + 1] - a;
+  // no qo_indptr: one query row per request, row r (a decode batch)
+  const int a = p.qo_indptr != nullptr ? p.qo_indptr[I.r] : I.r;
+  I.qo_len = p.qo_indptr != nullptr ? p.qo_indptr[I.r + 1] - a : 1;
   I.q0 = a + I.qt * p.tile_rows;
   I.rows = min(p.tile_rows, I.qo_len - I.qt * p.tile_rows);  // valid query rows
   I.kv = p.kv_len[I.r];
@@ -131,7 +132,8 @@ __device__ __forceinline__ PItem prefill_item_or_empty(const PrefillParams& p, i
 }
 
 __device__ __forceinline__ bool request_ok(const PrefillParams& p, int r) {
-  const int a = p.qo_indptr[r], b = p.qo_indptr[r + 1];
+  const int a = p.qo_indptr != nullptr ? p.qo_indptr[r] : r;
+  const int b = p.qo_indptr != nullptr ? p.qo_indptr[r + 1] : r + 1;
   const int n = p.kv_len[r];
   int code = 0;
   if (a < 0 || b < a || b > p.total_qo) code = PD_DEV_BAD_INDPTR;
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
   __syncthreads();
   for (int r = tid; r < p.batch; r += blockDim.x) {
     if (!request_ok(p, r)) continue;
-    const int qo = p.qo_indptr[r + 1] - p.qo_indptr[r], n = p.kv_len[r];
+    const int qo = p.qo_indptr != nullptr ? p.qo_indptr[r + 1] - p.qo_indptr[r] : 1, n = p.kv_len[r];
     for (int qt = 0; qt * p.tile_rows < qo; ++qt)
       atomicAdd(&hist[min(kv_tiles(qt, qo, n, p.causal, p.tile_rows), kBuckets - 1)], 1);
   }
@@ -234,7 +236,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
   __syncthreads();
   for (int r = tid; r < p.batch; r += blockDim.x) {
     if (!request_ok(p, r)) continue;
-    const int qo = p.qo_indptr[r + 1] - p.qo_indptr[r], n = p.kv_len[r];
+    const int qo = p.qo_indptr != nullptr ? p.qo_indptr[r + 1] - p.qo_indptr[r] : 1, n = p.kv_len[r];
     for (int qt = 0; qt * p.tile_rows < qo; ++qt) {
       const int pos = atomicAdd(&cursor[min(kv_tiles(qt, qo, n, p.causal, p.tile_rows), kBuckets - 1)], 1);
       if (pos < p.max_rq) p.rq_list[pos] = make_int2(r, qt);
@@ -736,6 +738,7 @@ int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const vo
       return PD_ERR_CUDA;
     configured_device = dev;
   }
+  last_kernel() = "prefill_kernel";
   prefill_plan_kernel<<<1, 1024, 0, stream>>>(p);
   int64_t grid = device_sm_count();
   const int64_t max_items = (int64_t)p.max_rq * p.item_heads;

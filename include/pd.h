@@ -159,7 +159,12 @@ PD_API size_t pd_attn_workspace_size(const pd_attn_desc *desc, const pd_batch *b
  * The KV axis is split into chunks processed by separate CTAs; the partial
  * results are merged by log-sum-exp. Supported: kv_dtype f32 or bf16, D 64 or
  * 128, any page size, any group size Hq/Hkv. The causal flag is irrelevant for
- * one row per request.
+ * one row per request. A large grouped-query batch (bf16, D 128, page size a
+ * power of two >= 8, group 2..128 dividing 128, no qo_indptr, and at least
+ * four (request, KV head) pairs per SM) instead runs on the tensor-core kernel
+ * of pd_attn_prefill with the group's query heads packed into one tile, which
+ * reads each KV tile once per group without splitting; the workspace size
+ * query covers both. Results agree within the stated tolerances either way.
  */
 PD_API int pd_attn_decode(const pd_attn_desc *desc, const pd_batch *batch, const void *q,
                    const void *k_pool, const void *v_pool, void *o, float *lse,
@@ -331,6 +336,15 @@ PD_API int pd_messenger_join(pd_messenger *m, int32_t *layers_sent);
  * PD_ERR_INVALID_ARG if exactly one of them is NULL.
  */
 PD_API int pd_profile_events(void *start_event, void *stop_event);
+
+/*
+ * Name of the main kernel the last call of this host thread launched
+ * ("decode_kernel", "prefill_kernel", "kv_pack_kernel", ...; "" before any
+ * call). Not part of the method: pd_attn_decode runs a large GQA batch on the
+ * tensor-core kernel and other batches on the split-KV kernel, and profiling
+ * needs to know which. The string is static.
+ */
+PD_API const char *pd_last_kernel(void);
 
 /* Static description of a pd_status or pd_device_status code (never NULL). */
 PD_API const char *pd_status_string(int32_t code);

@@ -128,3 +128,34 @@ def test_decode_many_requests_with_empty_ones():
     assert torch.all(o[empty] == 0) and torch.all(torch.isneginf(lse[empty]))
     o_ref, lse_ref = oracle.attention_case(case)
     compare(o, lse, o_ref, lse_ref, case.dtype)
+
+
+def test_large_gqa_batch_runs_packed_on_tensor_cores_and_others_split():
+    # the decode batch (128 requests x 8 KV heads) goes through the tensor-core
+    # kernel with 4 query heads per tile; a small batch and an MHA batch keep the
+    # split-KV kernel; all three match the oracle
+    big = wl.decode_batch()
+    check(big)
+    assert pd.pd_last_kernel() == "prefill_kernel"
+    small = wl.make_attn_case(108, [1] * 6, [4000, 17, 900, 2, 4096, 1000], 32, 8, 128, 16, wl.BF16)
+    check(small)
+    assert pd.pd_last_kernel() == "decode_kernel"
+    mha = wl.make_attn_case(109, [1] * 80, np.arange(80) * 7 + 1, 40, 40, 128, 16, wl.BF16)
+    check(mha)
+    assert pd.pd_last_kernel() == "decode_kernel"
+
+
+def test_tensor_core_decode_with_empty_and_short_requests():
+    # enough (request, KV head) pairs for the tensor-core path, with requests of
+    # no, one and a few keys among long ones
+    rng = np.random.default_rng(110)
+    kv = rng.integers(1, 3000, size=160)
+    kv[::13] = 0
+    kv[1::17] = 1
+    case = wl.make_attn_case(110, [1] * 160, kv, 32, 8, 128, 16, wl.BF16, causal=False)
+    o, lse = run_decode(case)
+    assert pd.pd_last_kernel() == "prefill_kernel"
+    empty = torch.from_numpy(kv == 0).cuda()
+    assert torch.all(o[empty] == 0) and torch.all(torch.isneginf(lse[empty]))
+    o_ref, lse_ref = oracle.attention_case(case)
+    compare(o, lse, o_ref, lse_ref, case.dtype)
