@@ -617,6 +617,12 @@ def profile_row(name: str, reps: int) -> None:
         else:
             fn = lambda: pd.pd_kv_append(w["k_new"], w["v_new"], w["k_pool"], w["v_pool"], w["qo_indptr"],
                                          w["kv_len"], w["page_indptr"], w["page_indices"], max_kv_len=512)
+    elif name == "decode_mha":
+        # the mixed workload's 63 decode requests (40 = 40 heads): the split-KV kernel
+        w = torch_gen.mixed_1p_nd()
+        pre = int(w["qo_len_host"][0])
+        fn = lambda: pd.pd_attn_decode(w["q"][pre:], w["k_pool"], w["v_pool"], w["kv_len"][1:], w["page_indptr"][1:],
+                                       w["page_indices"], max_kv_len=576)
     elif name == "mixed":
         w = torch_gen.mixed_1p_nd()
         fn = lambda: pd.pd_attn_mixed(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
@@ -647,7 +653,7 @@ def main():
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile-row", default=None,
-                    help="run only this row's call (decode, append, prefill, mixed, pack, unpack) for ncu")
+                    help="run only this row's call (decode, decode_mha, append, prefill, mixed, pack, unpack) for ncu")
     ap.add_argument("--profile-reps", type=int, default=3)
     args = ap.parse_args()
     if args.profile_row:
