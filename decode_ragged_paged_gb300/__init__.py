@@ -139,8 +139,13 @@ def _dtype_code(dt: torch.dtype) -> int:
     raise PdError(f"unsupported dtype {dt}")
 
 
-def _stream(stream) -> int | None:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, device: int | None = None) -> int | None:
     if stream is None:
+        if _raw_stream is not None and device is not None and device >= 0:
+            return _raw_stream(device)  # the current stream's handle, without building a Stream object
         return torch.cuda.current_stream().cuda_stream
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
@@ -189,12 +194,17 @@ def _attn(name, kind, q, k_pool, v_pool, kv_len, page_indptr, page_indices, qo_i
         lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
     elif lse is False:
         lse = None
-    need = pd_attn_workspace_size(desc, batch, kind)
-    if workspace is None or workspace.numel() < need:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    rc = getattr(lib, name)(ctypes.byref(desc), ctypes.byref(batch), _ptr(q), _ptr(k_pool), _ptr(v_pool),
-                            _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(dev_status),
-                            _stream(stream))
+    fn, dref, bref = getattr(lib, name), ctypes.byref(desc), ctypes.byref(batch)
+    ptrs = (_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(o), _ptr(lse))
+    status, strm = _ptr(dev_status), _stream(stream, q.get_device())
+    if workspace is None:
+        workspace = torch.empty(max(pd_attn_workspace_size(desc, batch, kind), 16), dtype=torch.uint8,
+                                device=q.device)
+    rc = fn(dref, bref, *ptrs, _ptr(workspace), workspace.numel(), status, strm)
+    if rc == PD_ERR_WORKSPACE:  # the caller's workspace is too small for this batch: use one that fits
+        workspace = torch.empty(max(pd_attn_workspace_size(desc, batch, kind), 16), dtype=torch.uint8,
+                                device=q.device)
+        rc = fn(dref, bref, *ptrs, _ptr(workspace), workspace.numel(), status, strm)
     _check(rc, name)
     return o, lse
 

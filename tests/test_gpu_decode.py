@@ -159,3 +159,19 @@ def test_tensor_core_decode_with_empty_and_short_requests():
     assert torch.all(o[empty] == 0) and torch.all(torch.isneginf(lse[empty]))
     o_ref, lse_ref = oracle.attention_case(case)
     compare(o, lse, o_ref, lse_ref, case.dtype)
+
+
+@pytest.mark.parametrize("big", [False, True])
+def test_binding_replaces_a_workspace_that_is_too_small(big):
+    # the binding passes the caller's workspace straight through; when the call
+    # reports it too small, it retries with one of pd_attn_workspace_size bytes
+    case = wl.decode_batch() if big else wl.make_attn_case(111, [1] * 6, [4000, 17, 900, 2, 4096, 1000],
+                                                          32, 8, 128, 16, wl.BF16)
+    d = DevCase(case)
+    tiny = torch.empty(16, dtype=torch.uint8, device="cuda")
+    o, lse = pd.pd_attn_decode(d.q, d.k_pool, d.v_pool, d.kv_len, d.page_indptr, d.page_indices,
+                               sm_scale=case.sm_scale, max_kv_len=d.max_kv_len, workspace=tiny)
+    torch.cuda.synchronize()
+    assert pd.pd_last_kernel() == ("prefill_kernel" if big else "decode_kernel")
+    o_ref, lse_ref = oracle.attention_case(case)
+    compare(o, lse, o_ref, lse_ref, case.dtype)
