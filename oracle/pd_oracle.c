@@ -17,13 +17,16 @@
  *   Same post, section "Sharded KV cache transfers" and its figure on NHD and
  *   HND layouts: inside a page the HND layout puts the head index before the
  *   token index, so page p holds [Hkv][page_size][head_dim].
+ *   The NHD layout of the same figure puts the token first: page p holds
+ *   [page_size][Hkv][head_dim]. Every function takes the layout of its pools.
  *   Same post, section "Qwen3-Coder": the model uses grouped-query attention,
  *   several query heads sharing one KV head.
  *
  *   For request r, query row i in [0, qo_len), query head h, KV head
  *   g = h / (Hq / Hkv) (contiguous groups), logical key j in [0, kv_len):
  *     page  = page_indices[page_indptr[r] + j / page_size], slot = j % page_size
- *     k_j   = k_pool[page][g][slot][:],  v_j likewise
+ *     k_j   = k_pool[page][g][slot][:] (HND) or k_pool[page][slot][g][:] (NHD),
+ *             v_j likewise
  *     s_j   = scale * <q_i,h , k_j>      for j <= kv_len - qo_len + i (causal,
  *             the new rows are the last qo_len positions), every j otherwise;
  *             masked keys get s_j = -inf
@@ -58,6 +61,17 @@
 #endif
 
 enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_HND = 0, ORACLE_NHD = 1 };
+
+/* element offset of (page, kv head g, slot, dim 0) in one pool:
+ * HND [page][Hkv][P][D], NHD [page][P][Hkv][D] */
+static int64_t pool_offset(int layout, int64_t page, int g, int slot, int hkv, int p, int d) {
+#if ORACLE_MUTANT == 12
+  layout = ORACLE_HND; /* planted: an NHD pool read as HND */
+#endif
+  if (layout == ORACLE_NHD) return ((page * p + slot) * (int64_t)hkv + g) * d;
+  return ((page * hkv + g) * (int64_t)p + slot) * d;
+}
 
 /* one stored element (fp32 or bf16 bit pattern) widened to fp64 */
 static double elem(const void *base, int64_t idx, int dtype) {
@@ -71,15 +85,15 @@ static double elem(const void *base, int64_t idx, int dtype) {
 }
 
 typedef struct {
-  int32_t batch, hq, hkv, d, p, dtype, causal;
+  int32_t batch, hq, hkv, d, p, dtype, causal, layout;
   double scale;
   const int32_t *qo_indptr, *kv_len, *page_indptr, *page_indices;
   const void *q, *k_pool, *v_pool;
 } attn_args;
 
-/* element offset of (page, kv head g, slot, dim 0) in an HND pool */
-static int64_t hnd_offset(const attn_args *a, int64_t page, int g, int slot) {
-  return ((page * a->hkv + g) * (int64_t)a->p + slot) * a->d;
+/* element offset of (page, kv head g, slot, dim 0) in the pools of a */
+static int64_t kv_offset(const attn_args *a, int64_t page, int g, int slot) {
+  return pool_offset(a->layout, page, g, slot, a->hkv, a->p, a->d);
 }
 
 /* physical page holding logical token j of request r */
@@ -132,7 +146,7 @@ static void attend_row(const attn_args *a, int r, int i, int h, double *o, doubl
       s[j] = -INFINITY;
       continue;
     }
-    const int64_t k_off = hnd_offset(a, page_of(a, r, j), g, slot_of(a, j));
+    const int64_t k_off = kv_offset(a, page_of(a, r, j), g, slot_of(a, j));
     double dot = 0.0;
     for (int dd = 0; dd < a->d; ++dd)
       dot += elem(a->q, q_off + dd, a->dtype) * elem(a->k_pool, k_off + dd, a->dtype);
@@ -155,7 +169,7 @@ static void attend_row(const attn_args *a, int r, int i, int h, double *o, doubl
 #else
     const void *vsrc = a->v_pool;
 #endif
-    const int64_t v_off = hnd_offset(a, page_of(a, r, j), g, slot_of(a, j));
+    const int64_t v_off = kv_offset(a, page_of(a, r, j), g, slot_of(a, j));
     for (int dd = 0; dd < a->d; ++dd) o[dd] += w * elem(vsrc, v_off + dd, a->dtype);
   }
   for (int dd = 0; dd < a->d; ++dd) o[dd] /= l;
@@ -168,6 +182,7 @@ static void attend_row(const attn_args *a, int r, int i, int h, double *o, doubl
 
 static int check_attn(const attn_args *a) {
   if (a->batch < 0 || a->hq <= 0 || a->hkv <= 0 || a->d <= 0 || a->p <= 0) return -1;
+  if (a->layout != ORACLE_HND && a->layout != ORACLE_NHD) return -1;
   if (a->hq % a->hkv != 0) return -1;
   for (int r = 0; r < a->batch; ++r) {
     const int qo = a->qo_indptr[r + 1] - a->qo_indptr[r];
@@ -197,9 +212,9 @@ static int threads_of(int nthreads) {
 int oracle_attention(int32_t batch, const int32_t *qo_indptr, const int32_t *kv_len,
                      const int32_t *page_indptr, const int32_t *page_indices, int32_t hq,
                      int32_t hkv, int32_t d, int32_t p, int32_t dtype, double scale,
-                     int32_t causal, const void *q, const void *k_pool, const void *v_pool,
-                     double *o, double *lse, int32_t nthreads) {
-  attn_args a = {batch, hq, hkv, d, p, dtype, causal, scale, qo_indptr, kv_len,
+                     int32_t causal, int32_t layout, const void *q, const void *k_pool,
+                     const void *v_pool, double *o, double *lse, int32_t nthreads) {
+  attn_args a = {batch, hq, hkv, d, p, dtype, causal, layout, scale, qo_indptr, kv_len,
                  page_indptr, page_indices, q, k_pool, v_pool};
   if (check_attn(&a)) return -1;
   int max_n = 1;
@@ -236,10 +251,10 @@ int oracle_attention(int32_t batch, const int32_t *qo_indptr, const int32_t *kv_
 int oracle_attention_rows(int32_t batch, const int32_t *qo_indptr, const int32_t *kv_len,
                           const int32_t *page_indptr, const int32_t *page_indices, int32_t hq,
                           int32_t hkv, int32_t d, int32_t p, int32_t dtype, double scale,
-                          int32_t causal, const void *q, const void *k_pool, const void *v_pool,
-                          int64_t n_sel, const int32_t *sel_row, const int32_t *sel_head,
-                          double *o, double *lse, int32_t nthreads) {
-  attn_args a = {batch, hq, hkv, d, p, dtype, causal, scale, qo_indptr, kv_len,
+                          int32_t causal, int32_t layout, const void *q, const void *k_pool,
+                          const void *v_pool, int64_t n_sel, const int32_t *sel_row,
+                          const int32_t *sel_head, double *o, double *lse, int32_t nthreads) {
+  attn_args a = {batch, hq, hkv, d, p, dtype, causal, layout, scale, qo_indptr, kv_len,
                  page_indptr, page_indices, q, k_pool, v_pool};
   if (check_attn(&a)) return -1;
   int max_n = 1;
@@ -276,10 +291,12 @@ int oracle_attention_rows(int32_t batch, const int32_t *qo_indptr, const int32_t
 /* Byte copies: append, pack, unpack. es = bytes per element.                 */
 /* ------------------------------------------------------------------------- */
 
-/* byte offset of (page, head, slot) in one layer's HND pool */
-static int64_t pool_row_bytes(int64_t page, int h, int slot, int hkv, int p, int d, int es) {
-  return (((page * hkv + h) * (int64_t)p + slot) * d) * es;
+/* byte offset of (page, head, slot) in one layer's pool */
+static int64_t pool_row_bytes(int layout, int64_t page, int h, int slot, int hkv, int p, int d, int es) {
+  return pool_offset(layout, page, h, slot, hkv, p, d) * es;
 }
+
+static int layout_ok(int32_t layout) { return layout == ORACLE_HND || layout == ORACLE_NHD; }
 
 /*
  * Append: new-token row idx (request r's token i, idx = new_indptr[r] + i) of
@@ -288,9 +305,10 @@ static int64_t pool_row_bytes(int64_t page, int h, int slot, int hkv, int p, int
  */
 int oracle_kv_append(int32_t batch, const int32_t *new_indptr, const int32_t *kv_len,
                      const int32_t *page_indptr, const int32_t *page_indices, int32_t num_pages,
-                     int32_t hkv, int32_t d, int32_t p, int32_t es, const void *k_new,
-                     const void *v_new, void *k_pool, void *v_pool) {
+                     int32_t hkv, int32_t d, int32_t p, int32_t es, int32_t layout,
+                     const void *k_new, const void *v_new, void *k_pool, void *v_pool) {
   const int64_t row_bytes = (int64_t)d * es;
+  if (!layout_ok(layout)) return -1;
   for (int r = 0; r < batch; ++r) {
     const int n_new = new_indptr[r + 1] - new_indptr[r];
     if (n_new < 0 || n_new > kv_len[r]) return -1;
@@ -308,7 +326,7 @@ int oracle_kv_append(int32_t batch, const int32_t *new_indptr, const int32_t *kv
       const int64_t src_row = (int64_t)new_indptr[r] + i;
       for (int h = 0; h < hkv; ++h) {
         const int64_t src = (src_row * hkv + h) * row_bytes;
-        const int64_t dst = pool_row_bytes(page, h, slot, hkv, p, d, es);
+        const int64_t dst = pool_row_bytes(layout, page, h, slot, hkv, p, d, es);
         memcpy((char *)k_pool + dst, (const char *)k_new + src, (size_t)row_bytes);
         memcpy((char *)v_pool + dst, (const char *)v_new + src, (size_t)row_bytes);
       }
@@ -329,6 +347,7 @@ static int64_t packed_row_bytes(int layer, int kv, int h, int64_t t, int64_t n, 
 /*
  * Pack: for every request r, layer, K/V, head h and token t < kv_len[r]:
  *   dst[dst_offsets[r] + packed(layer, kv, h, t)] = pool_layer,kv[page(r, t)][h][t % p]
+ * ([page(r, t)][t % p][h] for NHD pools)
  * where layer l's pools start at k_pool / v_pool + l * layer_stride bytes.
  */
 /*
@@ -355,10 +374,10 @@ static int pool_head(int32_t head_begin, int h) {
 int oracle_kv_pack(int32_t batch, const int32_t *kv_len, const int32_t *page_indptr,
                    const int32_t *page_indices, int32_t num_pages, int32_t num_layers,
                    int64_t layer_stride, int32_t hkv, int32_t head_begin, int32_t head_count, int32_t d,
-                   int32_t p, int32_t es, const void *k_pool, const void *v_pool, void *dst,
-                   const int64_t *dst_offsets) {
+                   int32_t p, int32_t es, int32_t layout, const void *k_pool, const void *v_pool,
+                   void *dst, const int64_t *dst_offsets) {
   const int64_t row_bytes = (int64_t)d * es;
-  if (!head_range_ok(hkv, head_begin, head_count)) return -1;
+  if (!head_range_ok(hkv, head_begin, head_count) || !layout_ok(layout)) return -1;
   for (int r = 0; r < batch; ++r) {
     const int64_t n = kv_len[r];
     if ((int64_t)(page_indptr[r + 1] - page_indptr[r]) * p < n) return -1;
@@ -369,7 +388,8 @@ int oracle_kv_pack(int32_t batch, const int32_t *kv_len, const int32_t *page_ind
           for (int64_t t = 0; t < n; ++t) {
             const int64_t page = page_indices[page_indptr[r] + t / p];
             if (page < 0 || page >= num_pages) return -1;
-            const int64_t src = pool_row_bytes(page, pool_head(head_begin, h), (int)(t % p), hkv, p, d, es);
+            const int64_t src =
+                pool_row_bytes(layout, page, pool_head(head_begin, h), (int)(t % p), hkv, p, d, es);
             const int64_t out = dst_offsets[r] + packed_row_bytes(layer, kv, h, t, n, head_count, d, es);
             memcpy((char *)dst + out, pool + src, (size_t)row_bytes);
           }
@@ -385,10 +405,10 @@ int oracle_kv_pack(int32_t batch, const int32_t *kv_len, const int32_t *page_ind
 int oracle_kv_unpack(int32_t batch, const int32_t *kv_len, const int32_t *page_indptr,
                      const int32_t *page_indices, int32_t num_pages, int32_t num_layers,
                      int64_t layer_stride, int32_t hkv, int32_t head_begin, int32_t head_count, int32_t d,
-                     int32_t p, int32_t es, const void *src, const int64_t *src_offsets, void *k_pool,
-                     void *v_pool) {
+                     int32_t p, int32_t es, int32_t layout, const void *src, const int64_t *src_offsets,
+                     void *k_pool, void *v_pool) {
   const int64_t row_bytes = (int64_t)d * es;
-  if (!head_range_ok(hkv, head_begin, head_count)) return -1;
+  if (!head_range_ok(hkv, head_begin, head_count) || !layout_ok(layout)) return -1;
   for (int r = 0; r < batch; ++r) {
     const int64_t n = kv_len[r];
     if ((int64_t)(page_indptr[r + 1] - page_indptr[r]) * p < n) return -1;
@@ -404,7 +424,7 @@ int oracle_kv_unpack(int32_t batch, const int32_t *kv_len, const int32_t *page_i
             const int64_t page = page_indices[page_indptr[r] + t / p];
             if (page < 0 || page >= num_pages) return -1;
             const int slot = (int)(t % p);
-            const int64_t dst = pool_row_bytes(page, pool_head(head_begin, h), slot, hkv, p, d, es);
+            const int64_t dst = pool_row_bytes(layout, page, pool_head(head_begin, h), slot, hkv, p, d, es);
             const int64_t in = src_offsets[r] + packed_row_bytes(layer, kv, h, t, n, head_count, d, es);
             memcpy(pool + dst, (const char *)src + in, (size_t)row_bytes);
           }

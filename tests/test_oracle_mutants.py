@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import workloads as wl
-from test_oracle_pins import brute_force, _two_key_case, _golden
+from test_oracle_pins import brute_force, _two_key_case, _golden, _nhd_golden_pools
 
 MUTANTS = {
     1: "scale dropped",
@@ -24,6 +24,7 @@ MUTANTS = {
     9: "unpack writes K into the V pool",
     10: "append writes new tokens in reverse order",
     11: "head range packed from the pool's first heads",
+    12: "NHD pools read as HND",
 }
 
 
@@ -32,6 +33,7 @@ def _attention_pins_hold(mutant):
         wl.make_attn_case(71, [1, 4, 1], [9, 12, 33], 4, 2, 8, 4, wl.F32, causal=True, num_pages=20),
         wl.make_attn_case(72, [6, 2], [6, 11], 4, 2, 16, 2, wl.BF16, causal=True, num_pages=20),
     ]
+    cases.append(wl.to_nhd(cases[0]))
     for case in cases:
         o, lse = oracle.attention_case(case, mutant=mutant)
         o_ref, lse_ref = brute_force(case)
@@ -54,6 +56,10 @@ def _copy_pins_hold(mutant):
                     k[0, page, h, s, d] = 1000 * page + 100 * h + 10 * s + d
     v = k + np.float32(0.5)
     packed = oracle.kv_pack([3], [0, 2], [2, 0], k, v, [0], 96, mutant=mutant)
+    if not np.array_equal(packed.view(np.float32), np.array(g["expected"], np.float32)):
+        return False
+    kn, vn = _nhd_golden_pools()
+    packed = oracle.kv_pack([3], [0, 2], [2, 0], kn, vn, [0], 96, mutant=mutant, layout=oracle.NHD)
     if not np.array_equal(packed.view(np.float32), np.array(g["expected"], np.float32)):
         return False
     hc = wl.kv_handoff(seed=81, batch=2, layers=2, heads=2, head_dim=4, src_page=4, dst_page=8,

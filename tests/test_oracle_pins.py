@@ -51,8 +51,12 @@ def brute_force(case):
         n = int(case.kv_len[r])
         qo = int(case.qo_indptr[r + 1] - case.qo_indptr[r])
         pages = case.table.page_indices[case.table.page_indptr[r]:case.table.page_indptr[r + 1]]
-        K = np.stack([kp[pages[t // P], :, t % P, :] for t in range(n)], axis=1) if n else np.zeros((case.num_kv_heads, 0, q.shape[2]))
-        V = np.stack([vp[pages[t // P], :, t % P, :] for t in range(n)], axis=1) if n else np.zeros((case.num_kv_heads, 0, q.shape[2]))
+        if case.layout == "NHD":   # page [P][Hkv][D]: slot first
+            at = lambda pool, t: pool[pages[t // P], t % P, :, :]
+        else:                      # page [Hkv][P][D]: head first
+            at = lambda pool, t: pool[pages[t // P], :, t % P, :]
+        K = np.stack([at(kp, t) for t in range(n)], axis=1) if n else np.zeros((case.num_kv_heads, 0, q.shape[2]))
+        V = np.stack([at(vp, t) for t in range(n)], axis=1) if n else np.zeros((case.num_kv_heads, 0, q.shape[2]))
         K = np.repeat(K, G, axis=0)            # [Hq][n][D]
         V = np.repeat(V, G, axis=0)
         Q = q[case.qo_indptr[r]:case.qo_indptr[r + 1]].transpose(1, 0, 2)  # [Hq][qo][D]
@@ -426,3 +430,83 @@ def test_head_range_outside_the_pool_is_rejected():
         with pytest.raises(ValueError):
             oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, hc.k_src, hc.v_src,
                            [0], 1024, head_begin=h0, head_count=cnt)
+
+
+# ---------------------------------------------------------------------------
+# NHD pools (post, "Sharded KV cache transfers": the figure contrasts NHD,
+# token before head, with HND, head before token)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("idx", range(4))
+def test_nhd_pools_match_brute_force_and_the_hnd_result(idx):
+    case = list(small_cases())[idx]
+    nhd = wl.to_nhd(case)
+    o, lse = oracle.attention_case(nhd)
+    o_bf, lse_bf = brute_force(nhd)
+    np.testing.assert_allclose(o, o_bf, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse, lse_bf, atol=1e-12, rtol=0)
+    o_h, lse_h = oracle.attention_case(case)
+    assert np.array_equal(o, o_h) and np.array_equal(lse, lse_h)  # same values, same order of sums
+
+
+def _nhd_golden_pools():
+    """The pack_small.txt pools written in the NHD layout: element (page, head h,
+    slot s, dim d) = 1000 page + 100 h + 10 s + d, stored at [page][s][h][d]."""
+    k = np.zeros((1, 3, 2, 2, 2), np.float32)
+    for page in range(3):
+        for s in range(2):
+            for h in range(2):
+                for d in range(2):
+                    k[0, page, s, h, d] = 1000 * page + 100 * h + 10 * s + d
+    return k, k + np.float32(0.5)
+
+
+def test_golden_pack_small_from_nhd_pools():
+    g = _golden("pack_small.txt")
+    k, v = _nhd_golden_pools()
+    packed = oracle.kv_pack([3], [0, 2], [2, 0], k, v, [0], 96, layout=oracle.NHD)
+    np.testing.assert_array_equal(packed.view(np.float32), np.array(g["expected"], np.float32))
+
+
+def test_nhd_append_pack_unpack_agree_with_hnd():
+    hc = wl.kv_handoff(seed=91, batch=3, layers=2, heads=3, head_dim=4, src_page=4, dst_page=8,
+                       dtype=wl.F32, kv_lens=[13, 1, 8], src_slack=2, dst_slack=1)
+    nhd = wl.to_nhd(hc)
+    total = wl.packed_bytes(hc.kv_len, 2, 3, 4, 4)
+    t = hc.src_table
+    a = oracle.kv_pack(hc.kv_len, t.page_indptr, t.page_indices, hc.k_src, hc.v_src, hc.dst_offsets, total)
+    b = oracle.kv_pack(hc.kv_len, t.page_indptr, t.page_indices, nhd.k_src, nhd.v_src, hc.dst_offsets, total,
+                       layout=oracle.NHD)
+    assert np.array_equal(a, b)
+    # unpack into page-8 pools of both layouts (NaN where no token lands)
+    dshape = (2, hc.dst_table.num_pages, 3, 8, 4)
+    kh, vh = np.full(dshape, np.nan, np.float32), np.full(dshape, np.nan, np.float32)
+    kn, vn = wl.nhd_pool(kh), wl.nhd_pool(vh)
+    d = hc.dst_table
+    oracle.kv_unpack(hc.kv_len, d.page_indptr, d.page_indices, a, hc.dst_offsets, kh, vh)
+    oracle.kv_unpack(hc.kv_len, d.page_indptr, d.page_indices, a, hc.dst_offsets, kn, vn, layout=oracle.NHD)
+    np.testing.assert_array_equal(wl.nhd_pool(kh), kn)
+    np.testing.assert_array_equal(wl.nhd_pool(vh), vn)
+    # append the last two tokens of every request into both layouts
+    case = wl.make_attn_case(92, [2, 1, 2], [13, 1, 8], 6, 3, 4, 4, wl.F32, with_new_tokens=True, num_pages=9)
+    ckn, cvn = wl.nhd_pool(case.k_pool), wl.nhd_pool(case.v_pool)
+    tt = case.table
+    oracle.kv_append(case.qo_indptr, case.kv_len, tt.page_indptr, tt.page_indices, case.k_new, case.v_new,
+                     case.k_pool, case.v_pool)
+    oracle.kv_append(case.qo_indptr, case.kv_len, tt.page_indptr, tt.page_indices, case.k_new, case.v_new,
+                     ckn, cvn, layout=oracle.NHD)
+    np.testing.assert_array_equal(wl.nhd_pool(case.k_pool), ckn)
+    np.testing.assert_array_equal(wl.nhd_pool(case.v_pool), cvn)
+    # and the appended NHD pools attend like the brute force over them
+    nhd_case = wl.to_nhd(case)
+    nhd_case.k_pool, nhd_case.v_pool = ckn, cvn
+    o, lse = oracle.attention_case(nhd_case)
+    o_bf, lse_bf = brute_force(nhd_case)
+    np.testing.assert_allclose(o, o_bf, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse, lse_bf, atol=1e-12, rtol=0)
+
+
+def test_unknown_layout_is_rejected():
+    case = next(small_cases())
+    with pytest.raises(ValueError):
+        oracle.attention_case(case.__class__(**{**case.__dict__, "layout": "HDN"}))

@@ -10,6 +10,8 @@ Layouts produced here (all C-contiguous numpy arrays):
 * ``q``            [total_qo][Hq][D]            rows of all requests, packed
 * ``k_pool``       [num_pages][Hkv][P][D]       HND pages ("head before token")
 * ``v_pool``       same as ``k_pool``
+  (``to_nhd`` turns a case's pools into [num_pages][P][Hkv][D], the NHD
+  layout, "token before head", by swapping the two axes; nothing else changes)
 * ``qo_indptr``    int32 [B+1]
 * ``kv_len``       int32 [B]
 * ``page_indptr``  int32 [B+1]
@@ -130,6 +132,7 @@ class AttnCase:
     k_new: np.ndarray | None = None
     v_new: np.ndarray | None = None
     meta: dict = field(default_factory=dict)
+    layout: str = "HND"        # "HND": pools [pages][Hkv][P][D]; "NHD": [pages][P][Hkv][D]
 
     @property
     def batch_size(self) -> int:
@@ -268,6 +271,7 @@ class HandoffCase:
     dst_page_size: int
     dst_table: PageTable
     dst_offsets: np.ndarray    # int64 [B], byte offset of each request's packed block
+    layout: str = "HND"        # of k_src / v_src: "NHD" holds [L][num_pages][P][Hkv][D]
 
 
 def kv_handoff(seed: int = 5, batch: int = 8, length: int = 512, layers: int = 40,
@@ -306,3 +310,21 @@ def packed_bytes(kv_len, num_layers: int, num_kv_heads: int, head_dim: int, elem
     """Bytes of K and V that a handoff moves: every logical token of every layer,
     head and dimension, for both K and V."""
     return int(np.sum(np.asarray(kv_len, dtype=np.int64))) * 2 * num_layers * num_kv_heads * head_dim * elem_size
+
+
+def nhd_pool(pool: np.ndarray) -> np.ndarray:
+    """An HND pool ([..][num_pages][Hkv][P][D]) with its head and slot axes swapped:
+    the same values in the NHD layout ([..][num_pages][P][Hkv][D])."""
+    return np.ascontiguousarray(np.swapaxes(pool, -3, -2))
+
+
+def to_nhd(case):
+    """A copy of an AttnCase or HandoffCase whose pools hold the same values in
+    the NHD layout. Page tables, lengths, q and new-token rows are shared."""
+    import dataclasses
+    if isinstance(case, AttnCase):
+        assert case.layout == "HND"
+        return dataclasses.replace(case, k_pool=nhd_pool(case.k_pool), v_pool=nhd_pool(case.v_pool),
+                                   layout="NHD")
+    assert case.layout == "HND"
+    return dataclasses.replace(case, k_src=nhd_pool(case.k_src), v_src=nhd_pool(case.v_src), layout="NHD")
