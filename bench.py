@@ -520,6 +520,23 @@ def measure_rows(args, dev, peaks) -> dict:
         rows["verify_decode"] = {"status": str(e)}
     del w
 
+    # the decode batch on NHD pools ([page][slot][head][dim]): same values, the
+    # head and slot axes of the pools swapped
+    w = torch_gen.decode_batch(device=dev)
+    nbytes = decode_bytes(w)
+    for key in ("k_pool", "v_pool"):
+        w[key] = w[key].transpose(1, 2).contiguous()
+    o = torch.empty_like(w["q"])
+    wsn = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+    ms, kms, hus = timed(lambda: pd.pd_attn_decode(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
+                                                   w["page_indices"], max_kv_len=4096, o=o, workspace=wsn,
+                                                   layout="NHD"), reps, warm, flush)
+    rows["decode_nhd"] = {"workload": WORKLOAD.replace("page_size 16", "page_size 16, NHD pools"),
+                          "kernel": pd.pd_last_kernel(), "ms": round(ms, 5), "kernel_ms": round(kms, 5),
+                          "host_us": round(hus, 1), "GBs": round(nbytes / kms / 1e6, 1),
+                          "frac_hbm": round(nbytes / kms / 1e6 / hbm, 4), "bound": "hbm", "bytes": nbytes}
+    del w, wsn
+
     w = torch_gen.kv_handoff(device=dev)
     byts = 2 * w["buffer"].numel()
     ms, kms, hus = timed(lambda: pd.pd_kv_pack(w["k_src"], w["v_src"], w["kv_len"], w["src_indptr"], w["src_indices"],
@@ -535,6 +552,26 @@ def measure_rows(args, dev, peaks) -> dict:
                       "GBs": round(byts / kms / 1e6, 1), "frac_hbm": round(byts / kms / 1e6 / hbm, 4),
                       "bound": "hbm", "bytes": byts}
     rows["layer_streamed_handoff"] = layer_streamed_row(w, reps=3)
+
+    # the same handoff with NHD pools on both sides (pool side read / written
+    # one head_dim row per token)
+    k_nhd = w["k_src"].transpose(2, 3).contiguous()
+    v_nhd = w["v_src"].transpose(2, 3).contiguous()
+    ms, kms, hus = timed(lambda: pd.pd_kv_pack(k_nhd, v_nhd, w["kv_len"], w["src_indptr"], w["src_indices"],
+                                               w["buffer"], w["offsets"], max_kv_len=512, layout="NHD"), reps, warm)
+    rows["pack_nhd"] = {"workload": "pack workload, NHD source pools", "ms": round(ms, 5), "kernel_ms": round(kms, 5),
+                        "host_us": round(hus, 1), "GBs": round(byts / kms / 1e6, 1),
+                        "frac_hbm": round(byts / kms / 1e6 / hbm, 4), "bound": "hbm", "bytes": byts}
+    del k_nhd, v_nhd
+    kd_nhd = w["k_dst"].transpose(2, 3).contiguous()
+    vd_nhd = w["v_dst"].transpose(2, 3).contiguous()
+    ms, kms, hus = timed(lambda: pd.pd_kv_unpack(w["buffer"], w["offsets"], kd_nhd, vd_nhd, w["kv_len"],
+                                                 w["dst_indptr"], w["dst_indices"], max_kv_len=512, layout="NHD"),
+                         reps, warm)
+    rows["unpack_nhd"] = {"workload": "unpack workload, NHD page-64 pool", "ms": round(ms, 5),
+                          "kernel_ms": round(kms, 5), "host_us": round(hus, 1), "GBs": round(byts / kms / 1e6, 1),
+                          "frac_hbm": round(byts / kms / 1e6 / hbm, 4), "bound": "hbm", "bytes": byts}
+    del kd_nhd, vd_nhd
 
     # sharded handoff (TP2 prefiller -> TP1 decoder): two blocks of 20 heads
     # unpacked into heads [0, 20) and [20, 40) of one 40-head pool

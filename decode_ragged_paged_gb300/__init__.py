@@ -9,7 +9,8 @@ call fails, an exception is raised.
 
 Tensor layouts (see ``include/pd.h``):
     q, o            [total_qo][Hq][D]        fp32 or bf16
-    k_pool, v_pool  [num_pages][Hkv][P][D]   HND pages
+    k_pool, v_pool  [num_pages][Hkv][P][D]   HND pages (layout="HND", the default)
+                    [num_pages][P][Hkv][D]   NHD pages (layout="NHD")
     qo_indptr       int32 [B+1]; kv_len int32 [B]; page_indptr int32 [B+1];
     page_indices    int32 [nnz]
     lse             fp32 [total_qo][Hq], natural log
@@ -27,7 +28,7 @@ LIB_PATH = os.path.join(_HERE, "libpd.so")
 
 PD_OK, PD_ERR_INVALID_ARG, PD_ERR_UNSUPPORTED, PD_ERR_WORKSPACE, PD_ERR_CUDA, PD_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 PD_F32, PD_BF16 = 0, 1
-PD_LAYOUT_HND = 0
+PD_LAYOUT_HND, PD_LAYOUT_NHD = 0, 1
 PD_KIND_DECODE, PD_KIND_PREFILL, PD_KIND_MIXED = 0, 1, 2
 DEVICE_STATUS = {0: "ok", 1: "bad indptr", 2: "bad length", 3: "bad page table", 4: "not a decode",
                  5: "timeout", 6: "bad offset"}
@@ -158,10 +159,23 @@ def _i32(t, name):
     return t
 
 
-def make_attn_desc(q, k_pool, *, causal=True, sm_scale=None, o_dtype=None) -> AttnDesc:
-    num_pages, hkv, page, d = k_pool.shape
+def _layout_code(layout) -> int:
+    codes = {"HND": PD_LAYOUT_HND, "NHD": PD_LAYOUT_NHD, PD_LAYOUT_HND: PD_LAYOUT_HND, PD_LAYOUT_NHD: PD_LAYOUT_NHD}
+    if layout not in codes:
+        raise PdError(f"unknown pool layout {layout!r}")
+    return codes[layout]
+
+
+def _pool_dims(pool, layout):
+    """(num_pages, Hkv, P, D) of a pool in `layout` ([..][pages][Hkv][P][D] or [..][pages][P][Hkv][D])."""
+    n, a, b, d = pool.shape[-4:]
+    return (n, a, b, d) if _layout_code(layout) == PD_LAYOUT_HND else (n, b, a, d)
+
+
+def make_attn_desc(q, k_pool, *, causal=True, sm_scale=None, o_dtype=None, layout="HND") -> AttnDesc:
+    num_pages, hkv, page, d = _pool_dims(k_pool, layout)
     return AttnDesc(q.shape[1], hkv, d, page, _dtype_code(q.dtype),
-                    _dtype_code(o_dtype if o_dtype is not None else q.dtype), PD_LAYOUT_HND,
+                    _dtype_code(o_dtype if o_dtype is not None else q.dtype), _layout_code(layout),
                     int(bool(causal)), float(sm_scale) if sm_scale else 0.0)
 
 
@@ -180,12 +194,12 @@ def pd_attn_workspace_size(desc: AttnDesc, batch: Batch, kind: int) -> int:
 
 
 def _attn(name, kind, q, k_pool, v_pool, kv_len, page_indptr, page_indices, qo_indptr, *, causal,
-          sm_scale, max_qo_len, max_kv_len, o, lse, o_dtype, workspace, dev_status, stream):
+          sm_scale, max_qo_len, max_kv_len, o, lse, o_dtype, workspace, dev_status, stream, layout):
     lib = load_library()
     for t, n in ((q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool")):
         if not t.is_cuda or not t.is_contiguous():
             raise PdError(f"{n} must be a contiguous CUDA tensor")
-    desc = make_attn_desc(q, k_pool, causal=causal, sm_scale=sm_scale, o_dtype=o_dtype)
+    desc = make_attn_desc(q, k_pool, causal=causal, sm_scale=sm_scale, o_dtype=o_dtype, layout=layout)
     batch = make_batch(kv_len, page_indptr, page_indices, k_pool.shape[0], qo_indptr=qo_indptr,
                        total_qo=q.shape[0], max_qo_len=max_qo_len, max_kv_len=max_kv_len)
     if o is None:
@@ -211,47 +225,50 @@ def _attn(name, kind, q, k_pool, v_pool, kv_len, page_indptr, page_indices, qo_i
 
 def pd_attn_decode(q, k_pool, v_pool, kv_len, page_indptr, page_indices, qo_indptr=None, *, sm_scale=None,
                    max_kv_len=None, o=None, lse=True, o_dtype=None, workspace=None, dev_status=None,
-                   stream=None):
+                   stream=None, layout="HND"):
     """Decode attention: one query row per request. Returns (o, lse)."""
     return _attn("pd_attn_decode", PD_KIND_DECODE, q, k_pool, v_pool, kv_len, page_indptr, page_indices,
                  qo_indptr, causal=True, sm_scale=sm_scale, max_qo_len=1, max_kv_len=max_kv_len, o=o,
-                 lse=lse, o_dtype=o_dtype, workspace=workspace, dev_status=dev_status, stream=stream)
+                 lse=lse, o_dtype=o_dtype, workspace=workspace, dev_status=dev_status, stream=stream,
+                 layout=layout)
 
 
 def pd_attn_prefill(q, k_pool, v_pool, kv_len, page_indptr, page_indices, qo_indptr, *, causal=True,
                     sm_scale=None, max_qo_len=None, max_kv_len=None, o=None, lse=True, o_dtype=None,
-                    workspace=None, dev_status=None, stream=None):
+                    workspace=None, dev_status=None, stream=None, layout="HND"):
     """Prefill attention over ragged query rows (qo_len <= kv_len). Returns (o, lse)."""
     if max_qo_len is None:
         max_qo_len = int((qo_indptr[1:] - qo_indptr[:-1]).max().item()) if qo_indptr.numel() > 1 else 0
     return _attn("pd_attn_prefill", PD_KIND_PREFILL, q, k_pool, v_pool, kv_len, page_indptr, page_indices,
                  qo_indptr, causal=causal, sm_scale=sm_scale, max_qo_len=max_qo_len, max_kv_len=max_kv_len,
-                 o=o, lse=lse, o_dtype=o_dtype, workspace=workspace, dev_status=dev_status, stream=stream)
+                 o=o, lse=lse, o_dtype=o_dtype, workspace=workspace, dev_status=dev_status, stream=stream,
+                 layout=layout)
 
 
 def pd_attn_mixed(q, k_pool, v_pool, kv_len, page_indptr, page_indices, qo_indptr, *, causal=True,
                   sm_scale=None, max_qo_len=None, max_kv_len=None, o=None, lse=True, o_dtype=None,
-                  workspace=None, dev_status=None, stream=None):
+                  workspace=None, dev_status=None, stream=None, layout="HND"):
     """Mixed prefill + decode batch in one launch. Returns (o, lse)."""
     if max_qo_len is None:
         max_qo_len = int((qo_indptr[1:] - qo_indptr[:-1]).max().item()) if qo_indptr.numel() > 1 else 0
     return _attn("pd_attn_mixed", PD_KIND_MIXED, q, k_pool, v_pool, kv_len, page_indptr, page_indices,
                  qo_indptr, causal=causal, sm_scale=sm_scale, max_qo_len=max_qo_len, max_kv_len=max_kv_len,
-                 o=o, lse=lse, o_dtype=o_dtype, workspace=workspace, dev_status=dev_status, stream=stream)
+                 o=o, lse=lse, o_dtype=o_dtype, workspace=workspace, dev_status=dev_status, stream=stream,
+                 layout=layout)
 
 
-def _kv_desc(pool, num_layers=1, layer_stride_bytes=0) -> KvDesc:
-    """pool: [num_pages][Hkv][P][D] or [L][num_pages][Hkv][P][D]."""
-    shape = pool.shape[-4:]
-    return KvDesc(shape[1], shape[3], shape[2], _dtype_code(pool.dtype), PD_LAYOUT_HND, int(num_layers),
+def _kv_desc(pool, num_layers=1, layer_stride_bytes=0, layout="HND") -> KvDesc:
+    """pool: [num_pages][Hkv][P][D] or [L][num_pages][Hkv][P][D] (HND); P and Hkv swapped for NHD."""
+    _, hkv, page, d = _pool_dims(pool, layout)
+    return KvDesc(hkv, d, page, _dtype_code(pool.dtype), _layout_code(layout), int(num_layers),
                   int(layer_stride_bytes))
 
 
 def pd_kv_append(k_new, v_new, k_pool, v_pool, new_indptr, kv_len, page_indptr, page_indices, *,
-                 max_kv_len=None, dev_status=None, stream=None):
+                 max_kv_len=None, dev_status=None, stream=None, layout="HND"):
     """Write new tokens' K/V rows ([total_new][Hkv][D]) into their page slots, in place."""
     lib = load_library()
-    desc = _kv_desc(k_pool)
+    desc = _kv_desc(k_pool, layout=layout)
     batch = make_batch(kv_len, page_indptr, page_indices, k_pool.shape[0], qo_indptr=_i32(new_indptr, "new_indptr"),
                        total_qo=k_new.shape[0], max_kv_len=max_kv_len)
     rc = lib.pd_kv_append(ctypes.byref(desc), ctypes.byref(batch), _ptr(k_new), _ptr(v_new), _ptr(k_pool),
@@ -266,11 +283,11 @@ def _layers(pools):
 
 
 def pd_kv_pack(k_pools, v_pools, kv_len, page_indptr, page_indices, dst, dst_offsets, *, max_kv_len=None,
-               dev_status=None, stream=None):
+               dev_status=None, stream=None, layout="HND"):
     """Gather every request's KV of all layers into dst (uint8) at dst_offsets (int64 bytes)."""
     lib = load_library()
     L, stride, num_pages = _layers(k_pools)
-    desc = _kv_desc(k_pools, L, stride)
+    desc = _kv_desc(k_pools, L, stride, layout)
     batch = make_batch(kv_len, page_indptr, page_indices, num_pages, max_kv_len=max_kv_len)
     rc = lib.pd_kv_pack(ctypes.byref(desc), ctypes.byref(batch), _ptr(k_pools), _ptr(v_pools), _ptr(dst),
                         dst.numel() * dst.element_size(), _ptr(dst_offsets), _ptr(dev_status), _stream(stream))
@@ -278,11 +295,11 @@ def pd_kv_pack(k_pools, v_pools, kv_len, page_indptr, page_indices, dst, dst_off
 
 
 def pd_kv_unpack(src, src_offsets, k_pools, v_pools, kv_len, page_indptr, page_indices, *, max_kv_len=None,
-                 dev_status=None, stream=None):
+                 dev_status=None, stream=None, layout="HND"):
     """Scatter packed per-request KV blocks into [L][num_pages][Hkv][P][D] pools, in place."""
     lib = load_library()
     L, stride, num_pages = _layers(k_pools)
-    desc = _kv_desc(k_pools, L, stride)
+    desc = _kv_desc(k_pools, L, stride, layout)
     batch = make_batch(kv_len, page_indptr, page_indices, num_pages, max_kv_len=max_kv_len)
     rc = lib.pd_kv_unpack(ctypes.byref(desc), ctypes.byref(batch), _ptr(src), src.numel() * src.element_size(),
                           _ptr(src_offsets), _ptr(k_pools), _ptr(v_pools), _ptr(dev_status), _stream(stream))
@@ -290,11 +307,11 @@ def pd_kv_unpack(src, src_offsets, k_pools, v_pools, kv_len, page_indptr, page_i
 
 
 def pd_kv_pack_heads(k_pools, v_pools, kv_len, page_indptr, page_indices, dst, dst_offsets, head_begin, head_count,
-                     *, max_kv_len=None, dev_status=None, stream=None):
+                     *, max_kv_len=None, dev_status=None, stream=None, layout="HND"):
     """pd_kv_pack of pool heads [head_begin, head_begin + head_count) only; blocks hold head_count heads."""
     lib = load_library()
     L, stride, num_pages = _layers(k_pools)
-    desc = _kv_desc(k_pools, L, stride)
+    desc = _kv_desc(k_pools, L, stride, layout)
     batch = make_batch(kv_len, page_indptr, page_indices, num_pages, max_kv_len=max_kv_len)
     rc = lib.pd_kv_pack_heads(ctypes.byref(desc), ctypes.byref(batch), int(head_begin), int(head_count),
                               _ptr(k_pools), _ptr(v_pools), _ptr(dst), dst.numel() * dst.element_size(),
@@ -303,11 +320,11 @@ def pd_kv_pack_heads(k_pools, v_pools, kv_len, page_indptr, page_indices, dst, d
 
 
 def pd_kv_unpack_heads(src, src_offsets, k_pools, v_pools, kv_len, page_indptr, page_indices, head_begin, head_count,
-                       *, max_kv_len=None, dev_status=None, stream=None):
+                       *, max_kv_len=None, dev_status=None, stream=None, layout="HND"):
     """pd_kv_unpack of blocks holding head_count heads into pool heads [head_begin, head_begin + head_count)."""
     lib = load_library()
     L, stride, num_pages = _layers(k_pools)
-    desc = _kv_desc(k_pools, L, stride)
+    desc = _kv_desc(k_pools, L, stride, layout)
     batch = make_batch(kv_len, page_indptr, page_indices, num_pages, max_kv_len=max_kv_len)
     rc = lib.pd_kv_unpack_heads(ctypes.byref(desc), ctypes.byref(batch), int(head_begin), int(head_count),
                                 _ptr(src), src.numel() * src.element_size(), _ptr(src_offsets), _ptr(k_pools),
@@ -316,11 +333,11 @@ def pd_kv_unpack_heads(src, src_offsets, k_pools, v_pools, kv_len, page_indptr, 
 
 
 def pd_kv_pack_layers(k_pools, v_pools, kv_len, page_indptr, page_indices, dst, dst_offsets, layer_begin,
-                      layer_count, *, max_kv_len=None, dev_status=None, stream=None):
+                      layer_count, *, max_kv_len=None, dev_status=None, stream=None, layout="HND"):
     """pd_kv_pack of layers [layer_begin, layer_begin + layer_count) into their places of the full blocks."""
     lib = load_library()
     L, stride, num_pages = _layers(k_pools)
-    desc = _kv_desc(k_pools, L, stride)
+    desc = _kv_desc(k_pools, L, stride, layout)
     batch = make_batch(kv_len, page_indptr, page_indices, num_pages, max_kv_len=max_kv_len)
     rc = lib.pd_kv_pack_layers(ctypes.byref(desc), ctypes.byref(batch), int(layer_begin), int(layer_count),
                                _ptr(k_pools), _ptr(v_pools), _ptr(dst), dst.numel() * dst.element_size(),
@@ -350,11 +367,12 @@ def pd_layer_signal(device_word, value: int, stream=None) -> None:
 
 
 def pd_messenger_start_pack(host_word, k_pools, v_pools, kv_len, page_indptr, page_indices, dst, dst_offsets, *,
-                            timeout_ms=1000, max_kv_len=None, dev_status=None, stream=None):
+                            timeout_ms=1000, max_kv_len=None, dev_status=None, stream=None,
+                            layout="HND"):
     """Start the host thread that packs each layer once the counter passes it; returns its handle."""
     lib = load_library()
     L, stride, num_pages = _layers(k_pools)
-    desc = _kv_desc(k_pools, L, stride)
+    desc = _kv_desc(k_pools, L, stride, layout)
     batch = make_batch(kv_len, page_indptr, page_indices, num_pages, max_kv_len=max_kv_len)
     handle = ctypes.c_void_p()
     rc = lib.pd_messenger_start_pack(ctypes.byref(handle), host_word, ctypes.byref(desc), ctypes.byref(batch),

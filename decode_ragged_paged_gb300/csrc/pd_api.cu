@@ -47,7 +47,7 @@ int check_attn(const pd_attn_desc* d, const pd_batch* b, bool need_qo_indptr) {
     return PD_ERR_INVALID_ARG;
   if (d->page_size <= 0 || d->head_dim <= 0) return PD_ERR_INVALID_ARG;
   if (elem_size(d->kv_dtype) == 0 || elem_size(d->o_dtype) == 0) return PD_ERR_INVALID_ARG;
-  if (d->layout != PD_LAYOUT_HND) return PD_ERR_UNSUPPORTED;
+  if (d->layout != PD_LAYOUT_HND && d->layout != PD_LAYOUT_NHD) return PD_ERR_INVALID_ARG;
   if (d->head_dim != 64 && d->head_dim != 128) return PD_ERR_UNSUPPORTED;
   if (!(d->sm_scale <= 0.f || isfinite(d->sm_scale))) return PD_ERR_INVALID_ARG;
   if (b->batch_size < 0 || b->total_qo < 0 || b->max_qo_len < 0 || b->max_kv_len < 0) return PD_ERR_INVALID_ARG;
@@ -110,6 +110,7 @@ int run_prefill(const pd_attn_desc* desc, const pd_batch* batch, int32_t max_qo_
   p.tile_heads = tile_heads;
   p.tile_rows = 128 / tile_heads;
   p.item_heads = p.hq / tile_heads;
+  p.nhd = desc->layout == PD_LAYOUT_NHD;
   p.scale_log2 = scale_of(desc) * kLog2e;
   p.qo_indptr = batch->qo_indptr;
   p.kv_len = batch->kv_len;
@@ -208,6 +209,7 @@ int pd_attn_decode(const pd_attn_desc* desc, const pd_batch* batch, const void* 
   p.head_dim = desc->head_dim;
   p.page_size = desc->page_size;
   p.group = p.hq / p.hkv;
+  p.nhd = desc->layout == PD_LAYOUT_NHD;
   p.heads_per_item = decode_heads_per_item(p.group, p.head_dim);
   p.items_per_chunk = p.hq / p.heads_per_item;
   p.total_qo = batch->total_qo;
@@ -269,7 +271,7 @@ int check_kv(const pd_kv_desc* d, const pd_batch* b) {
   const int es = elem_size(d->dtype);
   if (es == 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 || d->page_size <= 0 || d->num_layers <= 0)
     return PD_ERR_INVALID_ARG;
-  if (d->layout != PD_LAYOUT_HND) return PD_ERR_UNSUPPORTED;
+  if (d->layout != PD_LAYOUT_HND && d->layout != PD_LAYOUT_NHD) return PD_ERR_INVALID_ARG;
   if ((d->head_dim * es) % 16 != 0) return PD_ERR_UNSUPPORTED;
   if (d->num_layers > 1 && (d->layer_stride_bytes <= 0 || d->layer_stride_bytes % 16 != 0))
     return PD_ERR_INVALID_ARG;
@@ -290,6 +292,7 @@ KvCopyParams kv_params(const pd_kv_desc* d, const pd_batch* b, int32_t* status) 
   p.num_layers = d->num_layers;
   p.num_pages = b->num_pages;
   p.elem_size = elem_size(d->dtype);
+  p.nhd = d->layout == PD_LAYOUT_NHD;
   p.head_begin = 0;
   p.head_count = d->num_kv_heads;
   p.layer_begin = 0;

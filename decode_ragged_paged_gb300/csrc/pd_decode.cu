@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, PD_DECODE_MIN_BLOCKS) decode_kernel(
     // ---------------------------------------------------------- producer
     // Lanes 0..kPL-1 are independent producers: each walks the same item and
     // stage sequence and issues the stages that fall to it (one bulk copy per
-    // contiguous page run of the HND layout).
+    // contiguous page run of the HND layout, per token row of the NHD layout).
     uint32_t ctr = 0;
     if (lane < kPL) {
       const uint64_t policy = make_evict_first();
@@ -384,13 +384,17 @@ __global__ void __launch_bounds__(kThreads, PD_DECODE_MIN_BLOCKS) decode_kernel(
             mbar_arrive_expect_tx(&full[slot], (uint32_t)((t1 - t0) * RB));
             for (int t = t0; t < t1;) {
               const int slot_in_page = t % p.page_size;
-              const int run = min(t1 - t, p.page_size - slot_in_page);
+              // HND: the rest of the page's head slice is one run; NHD: one token row
+              // (slots of a head are hkv rows apart) unless there is a single head
+              const int run = (p.nhd && p.hkv > 1) ? 1 : min(t1 - t, p.page_size - slot_in_page);
               int32_t pid = __ldg(pages + t / p.page_size);
               if (pid < 0 || pid >= p.num_pages) {
                 report(p.status, PD_DEV_BAD_PAGE_TABLE);
                 pid = 0;
               }
-              const uint8_t* src = pool + (((int64_t)pid * p.hkv + I.g) * p.page_size + slot_in_page) * (int64_t)RB;
+              const int64_t row = p.nhd ? ((int64_t)pid * p.page_size + slot_in_page) * p.hkv + I.g
+                                        : ((int64_t)pid * p.hkv + I.g) * p.page_size + slot_in_page;
+              const uint8_t* src = pool + row * (int64_t)RB;
               bulk_g2s_hint(ring + (size_t)slot * SB + (size_t)(t - t0) * RB, src, (uint32_t)(run * RB), &full[slot],
                             policy);
               t += run;

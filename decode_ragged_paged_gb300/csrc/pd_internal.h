@@ -23,6 +23,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 //   part_lse  float[max_chunks][Hq]      their log2-sum-exp2 of scaled scores
 struct DecodeParams {
   int32_t batch, hq, hkv, head_dim, page_size, group, heads_per_item, items_per_chunk;
+  int32_t nhd;  // pools [page][slot][head][dim] instead of [page][head][slot][dim]
   int32_t total_qo, max_kv_len, num_pages, chunk_target, max_chunks;
   int32_t o_dtype;
   float scale_log2;  // softmax scale times log2(e)
@@ -70,6 +71,7 @@ struct PrefillParams {
   // heads of one KV head (tile_heads = the group, or 1); items per q tile =
   // item_heads = hq / tile_heads
   int32_t tile_heads, tile_rows, item_heads;
+  int32_t nhd;       // pools [page][slot][head][dim] instead of [page][head][slot][dim]
   float scale_log2;  // softmax scale times log2(e)
   const int32_t* qo_indptr;
   const int32_t* kv_len;
@@ -104,6 +106,7 @@ struct KvCopyParams {
   int32_t head_begin, head_count;    // pack / unpack: pool heads [head_begin, head_begin + head_count)
   int32_t layer_begin, layer_count;  // pack: layers [layer_begin, layer_begin + layer_count) of num_layers
   int32_t max_kv_len, max_new;
+  int32_t nhd;                       // pools [page][slot][head][dim] instead of [page][head][slot][dim]
   int64_t layer_stride;
   const int32_t* new_indptr;   // append only
   const int32_t* kv_len;
@@ -124,7 +127,8 @@ int launch_kv_unpack(const KvCopyParams& p, cudaStream_t stream);
 
 // ------------------------------------------------------------ tensor maps
 bool make_pool_map(CUtensorMap* map, const void* pool, int32_t dtype, int32_t num_pages, int32_t hkv,
-                   int32_t page_size, int32_t head_dim, int32_t box_cols, int32_t box_rows, bool swizzle128);
+                   int32_t page_size, int32_t head_dim, int32_t box_cols, int32_t box_rows, bool swizzle128,
+                   bool nhd = false);
 bool make_rows_map(CUtensorMap* map, const void* base, int32_t dtype, int32_t total, int32_t hq, int32_t head_dim,
                    int32_t box_cols, int32_t box_rows, bool swizzle128, int32_t box_heads = 1);
 

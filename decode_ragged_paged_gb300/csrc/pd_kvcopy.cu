@@ -9,8 +9,9 @@
 //   are split or rebuilt.
 //
 // All three are pure byte moves, bound by HBM bandwidth. Each unit of work is a
-// contiguous run on both sides and is copied by one warp with 16-byte vector
-// loads, several in flight per lane.
+// (page, head) slice, contiguous on both sides for HND pools and a run of
+// head_dim rows hkv rows apart on the pool side for NHD pools; one warp copies
+// it with 16-byte vector loads, several in flight per lane.
 #include "pd_common.cuh"
 #include "pd_internal.h"
 
@@ -52,20 +53,74 @@ __device__ __forceinline__ void warp_copy(const uint4* __restrict__ src, uint4* 
   }
 }
 
+// One warp copies `rows` rows of vpr 16-byte vectors; row i sits src_stride
+// vectors after row i-1 on the source side and dst_stride on the destination
+// side (a head's slots in an NHD pool are hkv rows apart).
+__device__ __forceinline__ void warp_copy_rows(const uint4* __restrict__ src, int64_t src_stride,
+                                               uint4* __restrict__ dst, int64_t dst_stride, int rows, int vpr,
+                                               int lane) {
+  if (src_stride == vpr && dst_stride == vpr) {
+    warp_copy(src, dst, rows * vpr, lane);
+    return;
+  }
+  const int nvec = rows * vpr;
+  // row of vector i: a shift when vpr is a power of two (every head_dim the
+  // benchmarks use), a division otherwise
+  const bool pow2 = (vpr & (vpr - 1)) == 0;
+  const int lg = __ffs(vpr) - 1;
+  for (int base = 0; base < nvec; base += 32 * kUnroll) {
+    uint4 t[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = base + u * 32 + lane;
+      if (i < nvec) {
+        const int r = pow2 ? i >> lg : i / vpr, c = i - r * vpr;
+        t[u] = ld_stream(src + r * src_stride + c);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = base + u * 32 + lane;
+      if (i < nvec) {
+        const int r = pow2 ? i >> lg : i / vpr, c = i - r * vpr;
+        st_stream(dst + r * dst_stride + c, t[u]);
+      }
+    }
+  }
+}
+
+// Vector offset of (page, head, slot) in one layer's pool, and the distance
+// between consecutive slots of one head.
+__device__ __forceinline__ int64_t pool_vec(const KvCopyParams& p, int64_t page, int h, int slot, int vpr) {
+  return (p.nhd ? (page * p.page_size + slot) * p.hkv + h : (page * p.hkv + h) * p.page_size + slot) * vpr;
+}
+__device__ __forceinline__ int64_t slot_stride_vec(const KvCopyParams& p, int vpr) {
+  return p.nhd ? (int64_t)p.hkv * vpr : vpr;
+}
+
 // Unit u of a pack / unpack enumerates (request r, layer, K/V, head h of the
-// range, page k of the request) with k fastest, so consecutive warps touch
-// consecutive bytes of the packed buffer. Page k carries tokens
-// [k*P, min((k+1)*P, kv_len)); packed head h is pool head head_begin + h.
+// range, page k of the request). Page k carries tokens [k*P, min((k+1)*P,
+// kv_len)); packed head h is pool head head_begin + h. For HND pools k is
+// fastest, so consecutive warps touch consecutive bytes of the packed buffer;
+// for NHD pools h is fastest, so consecutive warps cover the rows of one page,
+// which are contiguous in the pool.
 struct Unit {
   int r, layer, kv, h, k;
 };
 
-__device__ __forceinline__ Unit unit_of(int64_t u, int kp, int hkv, int layers) {
+__device__ __forceinline__ Unit unit_of(int64_t u, int kp, int hkv, int layers, bool head_fastest) {
   Unit x;
-  x.k = (int)(u % kp);
-  u /= kp;
-  x.h = (int)(u % hkv);
-  u /= hkv;
+  if (head_fastest) {
+    x.h = (int)(u % hkv);
+    u /= hkv;
+    x.k = (int)(u % kp);
+    u /= kp;
+  } else {
+    x.k = (int)(u % kp);
+    u /= kp;
+    x.h = (int)(u % hkv);
+    u /= hkv;
+  }
   x.kv = (int)(u % 2);
   u /= 2;
   x.layer = (int)(u % layers);
@@ -128,8 +183,7 @@ __global__ void __launch_bounds__(kCopyThreads) kv_append_kernel(const KvCopyPar
           const int kv = i / (p.hkv * vpr);
           const int rem = i - kv * p.hkv * vpr;
           const int h = rem / vpr, v = rem - h * vpr;
-          uint4* dst = static_cast<uint4*>(kv ? p.dst2 : p.dst) +
-                       (((int64_t)page * p.hkv + h) * p.page_size + slot) * vpr + v;
+          uint4* dst = static_cast<uint4*>(kv ? p.dst2 : p.dst) + pool_vec(p, page, h, slot, vpr) + v;
           *dst = tmp[u];
         }
       }
@@ -146,7 +200,7 @@ __global__ void __launch_bounds__(kCopyThreads) kv_pack_kernel(const KvCopyParam
   const int64_t units = (int64_t)p.batch * p.layer_count * 2 * p.head_count * kp;
   const int vpr = p.head_dim * p.elem_size / 16;
   for (int64_t u = warp0; u < units; u += nwarps) {
-    Unit x = unit_of(u, kp, p.head_count, p.layer_count);
+    Unit x = unit_of(u, kp, p.head_count, p.layer_count, p.nhd != 0);
     x.layer += p.layer_begin;  // blocks keep all num_layers layers
     const int n = __ldg(p.kv_len + x.r);
     if ((int64_t)x.k * p.page_size >= n) continue;
@@ -165,11 +219,10 @@ __global__ void __launch_bounds__(kCopyThreads) kv_pack_kernel(const KvCopyParam
     }
     const int rows = min(p.page_size, n - x.k * p.page_size);
     const uint8_t* pool = static_cast<const uint8_t*>(x.kv ? p.src2 : p.src) + (int64_t)x.layer * p.layer_stride;
-    const uint4* src =
-        reinterpret_cast<const uint4*>(pool) + ((int64_t)page * p.hkv + p.head_begin + x.h) * p.page_size * vpr;
+    const uint4* src = reinterpret_cast<const uint4*>(pool) + pool_vec(p, page, p.head_begin + x.h, 0, vpr);
     uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dst) + off) +
                  ((((int64_t)x.layer * 2 + x.kv) * p.head_count + x.h) * n + (int64_t)x.k * p.page_size) * vpr;
-    warp_copy(src, dst, rows * vpr, lane);
+    warp_copy_rows(src, slot_stride_vec(p, vpr), dst, vpr, rows, vpr, lane);
   }
 }
 
@@ -182,7 +235,7 @@ __global__ void __launch_bounds__(kCopyThreads) kv_unpack_kernel(const KvCopyPar
   const int64_t units = (int64_t)p.batch * p.num_layers * 2 * p.head_count * kp;
   const int vpr = p.head_dim * p.elem_size / 16;
   for (int64_t u = warp0; u < units; u += nwarps) {
-    const Unit x = unit_of(u, kp, p.head_count, p.num_layers);
+    const Unit x = unit_of(u, kp, p.head_count, p.num_layers, p.nhd != 0);
     const int n = __ldg(p.kv_len + x.r);
     if ((int64_t)x.k * p.page_size >= n) continue;
     const int pa = __ldg(p.page_indptr + x.r), pb = __ldg(p.page_indptr + x.r + 1);
@@ -200,10 +253,10 @@ __global__ void __launch_bounds__(kCopyThreads) kv_unpack_kernel(const KvCopyPar
     }
     const int rows = min(p.page_size, n - x.k * p.page_size);
     uint8_t* pool = static_cast<uint8_t*>(x.kv ? p.dst2 : p.dst) + (int64_t)x.layer * p.layer_stride;
-    uint4* dst = reinterpret_cast<uint4*>(pool) + ((int64_t)page * p.hkv + p.head_begin + x.h) * p.page_size * vpr;
+    uint4* dst = reinterpret_cast<uint4*>(pool) + pool_vec(p, page, p.head_begin + x.h, 0, vpr);
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.src) + off) +
                        ((((int64_t)x.layer * 2 + x.kv) * p.head_count + x.h) * n + (int64_t)x.k * p.page_size) * vpr;
-    warp_copy(src, dst, rows * vpr, lane);
+    warp_copy_rows(src, vpr, dst, slot_stride_vec(p, vpr), rows, vpr, lane);
   }
 }
 

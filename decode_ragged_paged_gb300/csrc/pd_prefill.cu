@@ -181,8 +181,10 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const TileB
   if (lane == 0) mbar_arrive_expect_tx(bar, kTileBytes);
   __syncwarp();
   if (lane < nb) {
-    tma_load_4d(dst + lane * pb * 128, map, 0, t.soff, g, t.pid, bar);
-    tma_load_4d(dst + kHalf + lane * pb * 128, map, 64, t.soff, g, t.pid, bar);
+    // the NHD map orders its coordinates (dim, head, slot, page), HND (dim, slot, head, page)
+    const int c1 = p.nhd ? g : t.soff, c2 = p.nhd ? t.soff : g;
+    tma_load_4d(dst + lane * pb * 128, map, 0, c1, c2, t.pid, bar);
+    tma_load_4d(dst + kHalf + lane * pb * 128, map, 64, c1, c2, t.pid, bar);
   }
 }
 
@@ -726,8 +728,8 @@ int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const vo
       !make_rows_map(&to, p.o, PD_BF16, p.total_qo, p.hq, kD, 64, p.tile_rows, true, p.tile_heads))
     return PD_ERR_CUDA;
   if (!make_rows_map(&tq, q, PD_BF16, p.total_qo, p.hq, kD, 64, p.tile_rows, true, p.tile_heads) ||
-      !make_pool_map(&tk, k_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true) ||
-      !make_pool_map(&tv, v_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true))
+      !make_pool_map(&tk, k_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true, p.nhd != 0) ||
+      !make_pool_map(&tv, v_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true, p.nhd != 0))
     return PD_ERR_CUDA;
   static int configured_device = -1;
   int dev = 0;

@@ -32,18 +32,30 @@ CUtensorMapDataType tma_dtype(int32_t dtype) {
 
 }  // namespace
 
-// Pool [num_pages][hkv][page_size][head_dim] as a 4-D tensor {head_dim, page_size,
-// hkv, num_pages} (innermost first); one box = box_rows slots x box_cols elements
-// of one (page, head).
+// HND pool [num_pages][hkv][page_size][head_dim] as a 4-D tensor {head_dim,
+// page_size, hkv, num_pages} (innermost first), box {box_cols, box_rows, 1, 1};
+// NHD pool [num_pages][page_size][hkv][head_dim] as {head_dim, hkv, page_size,
+// num_pages}, box {box_cols, 1, box_rows, 1}. Either way one box is box_rows
+// slots x box_cols elements of one (page, head), landing in shared memory as
+// box_rows rows of box_cols elements; coordinates follow the tensor's order.
 bool make_pool_map(CUtensorMap* map, const void* pool, int32_t dtype, int32_t num_pages, int32_t hkv,
-                   int32_t page_size, int32_t head_dim, int32_t box_cols, int32_t box_rows, bool swizzle128) {
+                   int32_t page_size, int32_t head_dim, int32_t box_cols, int32_t box_rows, bool swizzle128,
+                   bool nhd) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const int es = dtype == PD_BF16 ? 2 : 4;
+  const cuuint64_t row = (cuuint64_t)head_dim * es;
   cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)page_size, (cuuint64_t)hkv, (cuuint64_t)num_pages};
-  cuuint64_t strides[3] = {(cuuint64_t)head_dim * es, (cuuint64_t)page_size * head_dim * es,
-                           (cuuint64_t)hkv * page_size * head_dim * es};
+  cuuint64_t strides[3] = {row, (cuuint64_t)page_size * row, (cuuint64_t)hkv * page_size * row};
   cuuint32_t box[4] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1, 1};
+  if (nhd) {
+    dims[1] = (cuuint64_t)hkv;
+    dims[2] = (cuuint64_t)page_size;
+    strides[0] = row;                     // next head
+    strides[1] = (cuuint64_t)hkv * row;   // next slot
+    box[1] = 1;
+    box[2] = (cuuint32_t)box_rows;
+  }
   cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = fn(map, tma_dtype(dtype), 4, const_cast<void*>(pool), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,

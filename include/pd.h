@@ -23,11 +23,16 @@
  * the stream has passed the call. Descriptor structs are read on the host
  * during the call only.
  *
- * Pool layout (HND, "head before token", from the post's figure on NHD and HND
- * KV-cache layouts): a pool is [num_pages][num_kv_heads][page_size][head_dim],
- * row-major, so each head's slice of a page is one contiguous run of
- * page_size * head_dim elements. K and V live in two pools that share one page
- * table. Pools must be 16-byte aligned.
+ * Pool layouts (from the post's figure on NHD and HND KV-cache layouts):
+ *   PD_LAYOUT_HND, "head before token" (the default): a pool is
+ *     [num_pages][num_kv_heads][page_size][head_dim], row-major, so each head's
+ *     slice of a page is one contiguous run of page_size * head_dim elements;
+ *   PD_LAYOUT_NHD, "token before head": a pool is
+ *     [num_pages][page_size][num_kv_heads][head_dim], row-major, so each token's
+ *     heads are one contiguous run and a head's slots are num_kv_heads rows
+ *     apart.
+ * K and V live in two pools of the same layout that share one page table.
+ * Pools must be 16-byte aligned.
  *
  * Page table (CSR): request r owns pages
  * page_indices[page_indptr[r] .. page_indptr[r+1]); logical token t of r sits in
@@ -95,7 +100,7 @@ typedef enum {
 
 typedef enum { PD_F32 = 0, PD_BF16 = 1 } pd_dtype;
 
-typedef enum { PD_LAYOUT_HND = 0 } pd_layout;
+typedef enum { PD_LAYOUT_HND = 0, PD_LAYOUT_NHD = 1 } pd_layout;
 
 typedef enum { PD_KIND_DECODE = 0, PD_KIND_PREFILL = 1, PD_KIND_MIXED = 2 } pd_attn_kind;
 
@@ -107,7 +112,7 @@ typedef struct {
   int32_t page_size;    /* P: tokens per page, >= 1 */
   int32_t kv_dtype;     /* pd_dtype of q, k_pool and v_pool */
   int32_t o_dtype;      /* pd_dtype of o */
-  int32_t layout;       /* pd_layout; PD_LAYOUT_HND */
+  int32_t layout;       /* pd_layout of k_pool and v_pool */
   int32_t causal;       /* 1: bottom-right causal mask; 0: every row sees all kv_len keys */
   float sm_scale;       /* softmax scale; <= 0 selects 1/sqrt(head_dim) */
 } pd_attn_desc;
@@ -131,7 +136,7 @@ typedef struct {
   int32_t head_dim;           /* D; head_dim * element size must be a multiple of 16 bytes */
   int32_t page_size;          /* P >= 1 */
   int32_t dtype;              /* pd_dtype of the pools */
-  int32_t layout;             /* PD_LAYOUT_HND */
+  int32_t layout;             /* pd_layout of the pools */
   int32_t num_layers;         /* L >= 1 (append: the layer count is 1) */
   int64_t layer_stride_bytes; /* bytes from layer l's pool to layer l+1's; same for K and V */
 } pd_kv_desc;
@@ -232,8 +237,10 @@ PD_API int pd_kv_append(const pd_kv_desc *desc, const pd_batch *batch, const voi
  * KV pack (sections "KV Messenger" and "Sharded KV cache transfers": a
  * finished prefill's pages leave the prefiller). For every request r the
  * kv_len[r] tokens of every layer are gathered into a contiguous block at
- * dst + dst_offsets[r] bytes, laid out [L][2 (K, V)][Hkv][kv_len[r]][D]; with
- * the HND layout each (page, head) slice is one contiguous run on both sides.
+ * dst + dst_offsets[r] bytes, laid out [L][2 (K, V)][Hkv][kv_len[r]][D] for
+ * either pool layout (so an HND pool can hand off to an NHD pool); with the HND
+ * layout each (page, head) slice is one contiguous run on both sides, with NHD
+ * the pool side is read one head_dim row per token.
  * Layer l's pools start at k_pool / v_pool + l * layer_stride_bytes (device).
  * dst_offsets: device int64 [B], 16-byte multiples; dst_bytes: size of dst. A
  * request whose block would not fit inside dst is skipped and reported

@@ -60,7 +60,7 @@ def _batch(**kw):
     (dict(head_dim=96), pd.PD_ERR_UNSUPPORTED),
     (dict(page_size=0), pd.PD_ERR_INVALID_ARG),
     (dict(kv_dtype=7), pd.PD_ERR_INVALID_ARG),
-    (dict(layout=1), pd.PD_ERR_UNSUPPORTED),
+    (dict(layout=2), pd.PD_ERR_INVALID_ARG),     # neither HND (0) nor NHD (1)
 ])
 def test_decode_rejects_bad_descriptor(lib, kw, code):
     rc = lib.pd_attn_decode(ctypes.byref(_desc(**kw)), ctypes.byref(_batch()), 16, 16, 16, 16, None, 16, 1 << 30,
@@ -96,7 +96,7 @@ def test_kv_copies_reject_bad_descriptor(lib):
     bad = [pd.KvDesc(0, 128, 16, pd.PD_BF16, 0, 1, 0),            # no heads
            pd.KvDesc(2, 4, 16, pd.PD_BF16, 0, 1, 0),              # 8-byte rows
            pd.KvDesc(2, 128, 16, pd.PD_BF16, 0, 2, 8),            # unaligned layer stride
-           pd.KvDesc(2, 128, 16, pd.PD_BF16, 1, 1, 0)]            # NHD not built
+           pd.KvDesc(2, 128, 16, pd.PD_BF16, 2, 1, 0)]            # unknown layout
     for d in bad:
         assert lib.pd_kv_pack(ctypes.byref(d), ctypes.byref(b), 16, 16, 16, 1 << 20, 16, None, None) < 0
         assert lib.pd_kv_unpack(ctypes.byref(d), ctypes.byref(b), 16, 1 << 20, 16, 16, 16, None, None) < 0
