@@ -69,9 +69,12 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
                                            P, P, P, P]
             lib.oracle_kv_unpack.argtypes = [I32, P, P, P, I32, I32, I64, I32, I32, I32, I32, I32, I32, I32,
                                              P, P, P, P]
+            lib.oracle_mla_decode.argtypes = [I32, P, P, P, I32, I32, I32, I32, I32, D, P, P, I64, P, P, P, P,
+                                              I32]
             lib.oracle_num_threads.argtypes = [I32]
             for f in ("oracle_attention", "oracle_attention_rows", "oracle_kv_append",
-                      "oracle_kv_pack", "oracle_kv_unpack", "oracle_num_threads", "oracle_mutant"):
+                      "oracle_kv_pack", "oracle_kv_unpack", "oracle_mla_decode", "oracle_num_threads",
+                      "oracle_mutant"):
                 getattr(lib, f).restype = ctypes.c_int
             _LIBS[mutant] = lib
         return _LIBS[mutant]
@@ -213,6 +216,38 @@ def kv_unpack(kv_len, page_indptr, page_indices, src, src_offsets, k_pools, v_po
                                         _ptr(v_pools))
     if rc != 0:
         raise ValueError("oracle_kv_unpack rejected its inputs")
+
+
+def mla_decode(kv_len, page_indptr, page_indices, q, kv_pool, d_c, scale, sel_req=None, sel_head=None,
+               nthreads=0, mutant=0):
+    """MLA decode over a paged latent cache. q [B][Hq][d_c + d_r]; kv_pool
+    [num_pages][P][d_c + d_r]; scores over the whole row, values its first d_c
+    entries. All pairs: returns (o fp64 [B][Hq][d_c], lse fp64 [B][Hq]); with
+    sel_req / sel_head: (o [n][d_c], lse [n]) for those (request, head) pairs."""
+    kv_len = _i32(kv_len)
+    page_indptr, page_indices = _i32(page_indptr), _i32(page_indices)
+    q, kv_pool = np.ascontiguousarray(q), np.ascontiguousarray(kv_pool)
+    dt = _dtype_code(q)
+    assert _dtype_code(kv_pool) == dt
+    B, hq, w = q.shape
+    _, p, w2 = kv_pool.shape
+    assert w2 == w and 0 < d_c <= w
+    if sel_req is None:
+        n, sr, sh = 0, None, None
+        o = np.zeros((B, hq, d_c), dtype=np.float64)
+        lse = np.zeros((B, hq), dtype=np.float64)
+    else:
+        sr, sh = _i32(sel_req), _i32(sel_head)
+        n = len(sr)
+        o = np.zeros((n, d_c), dtype=np.float64)
+        lse = np.zeros(n, dtype=np.float64)
+    rc = _load(mutant).oracle_mla_decode(B, _ptr(kv_len), _ptr(page_indptr), _ptr(page_indices), hq, d_c,
+                                         w - d_c, p, dt, float(scale), _ptr(q), _ptr(kv_pool), n,
+                                         None if sr is None else _ptr(sr), None if sh is None else _ptr(sh),
+                                         _ptr(o), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_mla_decode rejected its inputs (rc={rc})")
+    return o, lse
 
 
 def attention_case(case, nthreads=0, mutant=0):

@@ -433,6 +433,107 @@ int oracle_kv_unpack(int32_t batch, const int32_t *kv_len, const int32_t *page_i
   return 0;
 }
 
+/* ------------------------------------------------------------------------- */
+/* MLA decode over a paged latent cache.                                      */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Perplexity, "Disaggregated prefill and decode" (2025), section
+ * "Disaggregated Deployments", "DeepSeek-R1": multi-head latent attention
+ * compresses the KV heads of a token into one latent vector that every query
+ * head reads, so the cache holds one vector per token and is never split by
+ * head. The pages give no formula; the reading taken is MLA's published
+ * decode form with the up-projections folded into q and o: the stored row of
+ * token j is c_j = [c_j^kv (d_c values) | k_j^rope (d_r values)], the query of
+ * head h is a row of d_c + d_r values, and
+ *   s_j = scale * <q_h, c_j>          over all d_c + d_r values
+ *   o_h = sum_j softmax(s)_j c_j^kv   over the first d_c values only
+ *   lse = m + ln(sum_j exp(s_j - m)).
+ * Pool: [num_pages][p][d_c + d_r]; page of token j as for attention. One query
+ * row per request; a request with no key gives o = 0, lse = -inf.
+ */
+static void mla_row(int32_t r, int32_t h, const int32_t *kv_len, const int32_t *page_indptr,
+                    const int32_t *page_indices, int32_t hq, int32_t d_c, int32_t d_r, int32_t p,
+                    int32_t dtype, double scale, const void *q, const void *kv_pool, double *o,
+                    double *lse, double *s) {
+  const int32_t w = d_c + d_r;
+  const int64_t n = kv_len[r];
+  const int64_t q_off = ((int64_t)r * hq + h) * w;
+#if ORACLE_MUTANT == 13
+  const int32_t score_dims = d_c; /* planted: the rope part left out of the scores */
+#else
+  const int32_t score_dims = w;
+#endif
+  double m = -INFINITY;
+  for (int64_t j = 0; j < n; ++j) {
+    const int64_t page = page_indices[page_indptr[r] + j / p];
+    const int64_t c_off = (page * p + j % p) * w;
+    double dot = 0.0;
+    for (int dd = 0; dd < score_dims; ++dd)
+      dot += elem(q, q_off + dd, dtype) * elem(kv_pool, c_off + dd, dtype);
+    s[j] = scale * dot;
+    if (s[j] > m) m = s[j];
+  }
+  for (int dd = 0; dd < d_c; ++dd) o[dd] = 0.0;
+  if (n == 0) {
+    *lse = -INFINITY;
+    return;
+  }
+  double l = 0.0;
+  for (int64_t j = 0; j < n; ++j) {
+    const double wt = exp(s[j] - m);
+    l += wt;
+    const int64_t page = page_indices[page_indptr[r] + j / p];
+    const int64_t c_off = (page * p + j % p) * w;
+    for (int dd = 0; dd < d_c; ++dd) o[dd] += wt * elem(kv_pool, c_off + dd, dtype);
+  }
+  for (int dd = 0; dd < d_c; ++dd) o[dd] /= l;
+  *lse = m + log(l);
+}
+
+/*
+ * All (request, head) pairs when sel_req is NULL (o: [batch][hq][d_c], lse:
+ * [batch][hq]); else the n_sel pairs (sel_req[k], sel_head[k]) (o: [n_sel][d_c],
+ * lse: [n_sel]). Returns 0, or -1 for inconsistent sizes.
+ */
+int oracle_mla_decode(int32_t batch, const int32_t *kv_len, const int32_t *page_indptr,
+                      const int32_t *page_indices, int32_t hq, int32_t d_c, int32_t d_r, int32_t p,
+                      int32_t dtype, double scale, const void *q, const void *kv_pool, int64_t n_sel,
+                      const int32_t *sel_req, const int32_t *sel_head, double *o, double *lse,
+                      int32_t nthreads) {
+  if (batch < 0 || hq <= 0 || d_c <= 0 || d_r < 0 || p <= 0) return -1;
+  int max_n = 1;
+  for (int r = 0; r < batch; ++r) {
+    if (kv_len[r] < 0 || (int64_t)(page_indptr[r + 1] - page_indptr[r]) * p < kv_len[r]) return -1;
+    if (kv_len[r] > max_n) max_n = kv_len[r];
+  }
+  const int64_t tasks = sel_req != NULL ? n_sel : (int64_t)batch * hq;
+  int err = 0;
+#pragma omp parallel num_threads(threads_of(nthreads))
+  {
+    double *s = (double *)malloc(sizeof(double) * (size_t)max_n);
+    if (!s) {
+#pragma omp atomic write
+      err = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t t = 0; t < tasks; ++t) {
+        const int r = sel_req != NULL ? sel_req[t] : (int)(t / hq);
+        const int h = sel_req != NULL ? sel_head[t] : (int)(t % hq);
+        if (r < 0 || r >= batch || h < 0 || h >= hq) {
+#pragma omp atomic write
+          err = 1;
+          continue;
+        }
+        mla_row(r, h, kv_len, page_indptr, page_indices, hq, d_c, d_r, p, dtype, scale, q, kv_pool,
+                o + t * d_c, lse + t, s);
+      }
+      free(s);
+    }
+  }
+  return err ? -1 : 0;
+}
+
 int oracle_num_threads(int32_t nthreads) { return threads_of(nthreads); }
 
 int oracle_mutant(void) { return ORACLE_MUTANT; }

@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import workloads as wl
-from test_oracle_pins import brute_force, _two_key_case, _golden, _nhd_golden_pools
+from test_oracle_pins import brute_force, _two_key_case, _golden, _nhd_golden_pools, mla_brute_force
 
 MUTANTS = {
     1: "scale dropped",
@@ -25,6 +25,7 @@ MUTANTS = {
     10: "append writes new tokens in reverse order",
     11: "head range packed from the pool's first heads",
     12: "NHD pools read as HND",
+    13: "MLA scores without the rope part",
 }
 
 
@@ -39,6 +40,12 @@ def _attention_pins_hold(mutant):
         o_ref, lse_ref = brute_force(case)
         if not (np.allclose(o, o_ref, atol=1e-12, rtol=0) and np.allclose(lse, lse_ref, atol=1e-12, rtol=0)):
             return False
+    mla = wl.mla_case(35, [9, 30, 2], num_qo_heads=4, d_c=16, d_r=8, page_size=4, dtype=wl.F32)
+    o, lse = oracle.mla_decode(mla.kv_len, mla.table.page_indptr, mla.table.page_indices, mla.q, mla.kv_pool,
+                               mla.d_c, mla.sm_scale, mutant=mutant)
+    o_ref, lse_ref = mla_brute_force(mla)
+    if not (np.allclose(o, o_ref, atol=1e-12, rtol=0) and np.allclose(lse, lse_ref, atol=1e-12, rtol=0)):
+        return False
     case, g = _two_key_case(2)
     o, lse = oracle.attention_case(case, mutant=mutant)
     if not (np.allclose(o[1, 0], g["row1_o"], atol=1e-15) and np.isclose(lse[1, 0], g["row1_lse"][0], atol=1e-15)):

@@ -510,3 +510,98 @@ def test_unknown_layout_is_rejected():
     case = next(small_cases())
     with pytest.raises(ValueError):
         oracle.attention_case(case.__class__(**{**case.__dict__, "layout": "HDN"}))
+
+
+# ---------------------------------------------------------------------------
+# MLA decode over a paged latent cache (post, "Disaggregated Deployments",
+# "DeepSeek-R1": one latent vector per token shared by every head)
+# ---------------------------------------------------------------------------
+
+def _mla_small(seed=31, dtype=wl.F32):
+    return wl.mla_case(seed, [5, 0, 17, 1, 40], num_qo_heads=6, d_c=32, d_r=8, page_size=4, dtype=dtype,
+                       num_pages=40)
+
+
+def _mla_oracle(c, mutant=0):
+    return oracle.mla_decode(c.kv_len, c.table.page_indptr, c.table.page_indices, c.q, c.kv_pool, c.d_c,
+                             c.sm_scale, mutant=mutant)
+
+
+def mla_brute_force(c):
+    """numpy fp64: gather each request's latent rows token by token, dense softmax."""
+    q, pool = _values(c.q), _values(c.kv_pool)
+    B, H, W = q.shape
+    o, lse = np.zeros((B, H, c.d_c)), np.full((B, H), -np.inf)
+    for r in range(B):
+        n = int(c.kv_len[r])
+        if n == 0:
+            continue
+        pages = c.table.page_indices[c.table.page_indptr[r]:c.table.page_indptr[r + 1]]
+        C = np.stack([pool[pages[t // c.page_size], t % c.page_size] for t in range(n)])  # [n][W]
+        S = q[r] @ C.T * c.sm_scale                                                        # [H][n]
+        m = S.max(axis=1, keepdims=True)
+        E = np.exp(S - m)
+        o[r] = (E @ C[:, :c.d_c]) / E.sum(axis=1, keepdims=True)
+        lse[r] = m[:, 0] + np.log(E.sum(axis=1))
+    return o, lse
+
+
+@pytest.mark.parametrize("dtype", [wl.F32, wl.BF16])
+def test_mla_matches_brute_force(dtype):
+    c = _mla_small(dtype=dtype)
+    o, lse = _mla_oracle(c)
+    o_bf, lse_bf = mla_brute_force(c)
+    np.testing.assert_allclose(o, o_bf, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse, lse_bf, atol=1e-12, rtol=0)
+
+
+def test_mla_is_attention_with_one_shared_head_and_zeroed_rope_values():
+    # the pinned attention oracle with Hkv = 1, head_dim d_c + d_r: keys are the
+    # whole latent row, values the same row with its rope part zeroed
+    c = _mla_small()
+    B, H, W = c.q.shape
+    k_pool = c.kv_pool[:, None, :, :].copy()           # [pages][1][P][W] (HND, one head)
+    v_pool = k_pool.copy()
+    v_pool[..., c.d_c:] = 0
+    qo_indptr = np.arange(B + 1, dtype=np.int32)
+    o_a, lse_a = oracle.attention(qo_indptr, c.kv_len, c.table.page_indptr, c.table.page_indices, c.q, k_pool,
+                                  v_pool, H, 1, c.sm_scale, causal=False)
+    o, lse = _mla_oracle(c)
+    np.testing.assert_allclose(o, o_a[:, :, :c.d_c], atol=1e-13, rtol=0)
+    assert np.all(o_a[:, :, c.d_c:] == 0)
+    np.testing.assert_allclose(lse, lse_a, atol=1e-13, rtol=0)
+
+
+def test_mla_matches_torch_sdpa_with_a_narrower_value():
+    c = _mla_small(seed=32)
+    o, lse = _mla_oracle(c)
+    q, pool = torch.from_numpy(_values(c.q)), torch.from_numpy(_values(c.kv_pool))
+    for r in range(c.batch_size):
+        n = int(c.kv_len[r])
+        if n == 0:
+            continue
+        pages = torch.from_numpy(c.table.page_indices[c.table.page_indptr[r]:c.table.page_indptr[r + 1]].astype(np.int64))
+        C = pool[pages].reshape(-1, pool.shape[-1])[:n]          # [n][W], pages in order
+        ref = torch.nn.functional.scaled_dot_product_attention(q[r][None, :, None, :], C[None, None],
+                                                               C[None, None, :, :c.d_c], scale=c.sm_scale)
+        np.testing.assert_allclose(o[r], ref[0, :, 0].numpy(), atol=1e-12, rtol=0)
+
+
+def test_mla_single_key_returns_its_latent_part():
+    c = wl.mla_case(33, [1, 1], num_qo_heads=3, d_c=16, d_r=8, page_size=2, dtype=wl.F32)
+    o, lse = _mla_oracle(c)
+    for r in range(2):
+        page = c.table.page_indices[c.table.page_indptr[r]]
+        row = c.kv_pool[page, 0].astype(np.float64)
+        np.testing.assert_array_equal(o[r], np.broadcast_to(row[:16], (3, 16)))
+        np.testing.assert_allclose(lse[r], c.sm_scale * (c.q[r].astype(np.float64) @ row), atol=1e-12)
+
+
+def test_mla_selected_pairs_equal_the_full_result():
+    c = _mla_small(seed=34)
+    o, lse = _mla_oracle(c)
+    sel_r, sel_h = np.array([4, 0, 2, 4]), np.array([5, 0, 3, 1])
+    o_s, lse_s = oracle.mla_decode(c.kv_len, c.table.page_indptr, c.table.page_indices, c.q, c.kv_pool, c.d_c,
+                                   c.sm_scale, sel_req=sel_r, sel_head=sel_h)
+    np.testing.assert_array_equal(o_s, o[sel_r, sel_h])
+    np.testing.assert_array_equal(lse_s, lse[sel_r, sel_h])

@@ -328,3 +328,51 @@ def to_nhd(case):
                                    layout="NHD")
     assert case.layout == "HND"
     return dataclasses.replace(case, k_src=nhd_pool(case.k_src), v_src=nhd_pool(case.v_src), layout="NHD")
+
+
+@dataclass
+class MlaCase:
+    """A decode batch over a paged latent cache (one row per token shared by all
+    query heads): q [B][Hq][d_c + d_r], kv_pool [num_pages][P][d_c + d_r]."""
+
+    dtype: str
+    num_qo_heads: int
+    d_c: int                   # latent (value) width
+    d_r: int                   # decoupled rope width, scores only
+    page_size: int
+    kv_len: np.ndarray
+    table: PageTable
+    q: np.ndarray
+    kv_pool: np.ndarray
+    sm_scale: float
+
+    @property
+    def batch_size(self) -> int:
+        return len(self.kv_len)
+
+
+def mla_case(seed: int, kv_lens, num_qo_heads: int = 128, d_c: int = 512, d_r: int = 64, page_size: int = 64,
+             dtype: str = BF16, num_pages: int | None = None, sm_scale: float = 192 ** -0.5) -> MlaCase:
+    """Seeded MLA decode batch. Draw order from one default_rng(seed) stream: the
+    page permutation, the latent pool, then q; slots holding no token are then
+    poisoned. The default scale is 1/sqrt(192), DeepSeek-V3's query-key head size
+    (128 + 64) before its up-projections are folded into q."""
+    rng = np.random.default_rng(seed)
+    kv = np.asarray(kv_lens, dtype=np.int64)
+    table = random_page_table(rng, kv, page_size, num_pages)
+    w = d_c + d_r
+    pool = _draw(rng, (table.num_pages, page_size, w), dtype)
+    q = _draw(rng, (len(kv), num_qo_heads, w), dtype)
+    pg, sl, _, _ = logical_slots(table, kv, page_size)
+    used = np.zeros((table.num_pages, page_size), dtype=bool)
+    used[pg, sl] = True
+    pool[~used] = _poison((), dtype)
+    return MlaCase(dtype, num_qo_heads, d_c, d_r, page_size, kv.astype(np.int32), table, q, pool, float(sm_scale))
+
+
+def mla_decode_batch(seed: int = 7, batch: int = 128, kv_lo: int = 512, kv_hi: int = 4096) -> MlaCase:
+    """128 decode requests, kv_len U[512, 4096], 128 query heads over a 512 + 64
+    latent row (DeepSeek-V3/R1 shapes with data-parallel attention: every head
+    on one GPU), page 64, bf16."""
+    kv = np.random.default_rng(seed + 1000).integers(kv_lo, kv_hi + 1, size=batch)
+    return mla_case(seed, kv)
