@@ -35,7 +35,7 @@ DEVICE_STATUS = {0: "ok", 1: "bad indptr", 2: "bad length", 3: "bad page table",
 
 # Every symbol include/pd.h declares.
 EXPORTS = ("pd_attn_workspace_size", "pd_attn_decode", "pd_attn_decode_static", "pd_attn_prefill",
-           "pd_attn_mixed",
+           "pd_attn_mixed", "pd_mla_workspace_size", "pd_mla_decode",
            "pd_kv_append", "pd_kv_pack", "pd_kv_unpack", "pd_kv_pack_heads", "pd_kv_unpack_heads",
            "pd_kv_pack_layers", "pd_counter_alloc", "pd_counter_free", "pd_layer_signal",
            "pd_messenger_start_pack", "pd_messenger_join",
@@ -70,6 +70,12 @@ class KvDesc(ctypes.Structure):
                 ("num_layers", ctypes.c_int32), ("layer_stride_bytes", ctypes.c_int64)]
 
 
+class MlaDesc(ctypes.Structure):
+    _fields_ = [("num_qo_heads", ctypes.c_int32), ("kv_lora_rank", ctypes.c_int32), ("rope_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("kv_dtype", ctypes.c_int32), ("o_dtype", ctypes.c_int32),
+                ("sm_scale", ctypes.c_float)]
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -89,6 +95,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                 getattr(lib, name).restype = ctypes.c_int
             lib.pd_attn_workspace_size.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(Batch), I32]
             lib.pd_attn_workspace_size.restype = S
+            lib.pd_mla_workspace_size.argtypes = [ctypes.POINTER(MlaDesc), ctypes.POINTER(Batch)]
+            lib.pd_mla_workspace_size.restype = S
+            lib.pd_mla_decode.argtypes = [ctypes.POINTER(MlaDesc), ctypes.POINTER(Batch), P, P, P, P, P, S, P, P]
+            lib.pd_mla_decode.restype = ctypes.c_int
             lib.pd_kv_append.argtypes = [ctypes.POINTER(KvDesc), ctypes.POINTER(Batch), P, P, P, P, P, P]
             lib.pd_kv_pack.argtypes = [ctypes.POINTER(KvDesc), ctypes.POINTER(Batch), P, P, P, S, P, P, P]
             lib.pd_kv_unpack.argtypes = [ctypes.POINTER(KvDesc), ctypes.POINTER(Batch), P, S, P, P, P, P, P]
@@ -255,6 +265,44 @@ def pd_attn_mixed(q, k_pool, v_pool, kv_len, page_indptr, page_indices, qo_indpt
                  qo_indptr, causal=causal, sm_scale=sm_scale, max_qo_len=max_qo_len, max_kv_len=max_kv_len,
                  o=o, lse=lse, o_dtype=o_dtype, workspace=workspace, dev_status=dev_status, stream=stream,
                  layout=layout)
+
+
+def pd_mla_decode(q, kv_pool, kv_len, page_indptr, page_indices, *, kv_lora_rank=512, sm_scale=None,
+                  max_kv_len=None, o=None, lse=True, o_dtype=None, workspace=None, dev_status=None, stream=None):
+    """MLA decode over a paged latent cache: q [B][Hq][kv_lora_rank + rope_dim], kv_pool
+    [num_pages][P][kv_lora_rank + rope_dim]; scores over the whole row, values its first
+    kv_lora_rank entries. Returns (o [B][Hq][kv_lora_rank], lse [B][Hq])."""
+    lib = load_library()
+    for t, n in ((q, "q"), (kv_pool, "kv_pool")):
+        if not t.is_cuda or not t.is_contiguous():
+            raise PdError(f"{n} must be a contiguous CUDA tensor")
+    B, hq, w = q.shape
+    num_pages, page, w2 = kv_pool.shape
+    if w2 != w:
+        raise PdError("q and kv_pool rows differ in width")
+    desc = MlaDesc(hq, int(kv_lora_rank), w - int(kv_lora_rank), page, _dtype_code(q.dtype),
+                   _dtype_code(o_dtype if o_dtype is not None else q.dtype), float(sm_scale) if sm_scale else 0.0)
+    batch = make_batch(kv_len, page_indptr, page_indices, num_pages, total_qo=B, max_kv_len=max_kv_len)
+    if o is None:
+        o = torch.empty((B, hq, int(kv_lora_rank)), dtype=o_dtype if o_dtype is not None else q.dtype,
+                        device=q.device)
+    if lse is True:
+        lse = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+    elif lse is False:
+        lse = None
+    dref, bref = ctypes.byref(desc), ctypes.byref(batch)
+    args = (_ptr(q), _ptr(kv_pool), _ptr(o), _ptr(lse))
+    status, strm = _ptr(dev_status), _stream(stream, q.get_device())
+    if workspace is None:
+        workspace = torch.empty(max(int(lib.pd_mla_workspace_size(dref, bref)), 16), dtype=torch.uint8,
+                                device=q.device)
+    rc = lib.pd_mla_decode(dref, bref, *args, _ptr(workspace), workspace.numel(), status, strm)
+    if rc == PD_ERR_WORKSPACE:  # the caller's workspace is too small for this batch: use one that fits
+        workspace = torch.empty(max(int(lib.pd_mla_workspace_size(dref, bref)), 16), dtype=torch.uint8,
+                                device=q.device)
+        rc = lib.pd_mla_decode(dref, bref, *args, _ptr(workspace), workspace.numel(), status, strm)
+    _check(rc, "pd_mla_decode")
+    return o, lse
 
 
 def _kv_desc(pool, num_layers=1, layer_stride_bytes=0, layout="HND") -> KvDesc:

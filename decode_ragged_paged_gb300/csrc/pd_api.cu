@@ -266,6 +266,66 @@ int pd_attn_mixed(const pd_attn_desc* desc, const pd_batch* batch, const void* q
 
 namespace {
 
+int check_mla(const pd_mla_desc* d, const pd_batch* b) {
+  if (d == nullptr || b == nullptr) return PD_ERR_INVALID_ARG;
+  if (d->num_qo_heads <= 0 || d->kv_lora_rank <= 0 || d->rope_dim < 0 || d->page_size <= 0)
+    return PD_ERR_INVALID_ARG;
+  if (elem_size(d->kv_dtype) == 0 || elem_size(d->o_dtype) == 0) return PD_ERR_INVALID_ARG;
+  if (!(d->sm_scale <= 0.f || isfinite(d->sm_scale))) return PD_ERR_INVALID_ARG;
+  if (b->batch_size < 0 || b->max_kv_len < 0) return PD_ERR_INVALID_ARG;
+  if (b->batch_size > 0) {
+    if (b->kv_len == nullptr || b->page_indptr == nullptr || b->page_indices == nullptr) return PD_ERR_INVALID_ARG;
+    if (b->num_pages <= 0) return PD_ERR_INVALID_ARG;
+  }
+  if (mla_pairs() < 1) return PD_ERR_CUDA;
+  return mla_supported(d->kv_lora_rank, d->rope_dim, d->kv_dtype, d->num_qo_heads, d->page_size);
+}
+
+}  // namespace
+
+size_t pd_mla_workspace_size(const pd_mla_desc* desc, const pd_batch* batch) {
+  if (check_mla(desc, batch) != PD_OK) return 0;
+  return mla_layout(batch->batch_size, desc->num_qo_heads).total;
+}
+
+int pd_mla_decode(const pd_mla_desc* desc, const pd_batch* batch, const void* q, const void* kv_pool, void* o,
+                  float* lse, void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  const int rc = check_mla(desc, batch);
+  if (rc != PD_OK) return rc;
+  if (batch->batch_size == 0) return PD_OK;
+  if (q == nullptr || kv_pool == nullptr || o == nullptr || workspace == nullptr) return PD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(o) || !aligned16(workspace)) return PD_ERR_INVALID_ARG;
+  const MlaLayout L = mla_layout(batch->batch_size, desc->num_qo_heads);
+  if (workspace_bytes < L.total) return PD_ERR_WORKSPACE;
+  MlaParams p{};
+  p.batch = batch->batch_size;
+  p.hq = desc->num_qo_heads;
+  p.page_size = desc->page_size;
+  p.num_pages = batch->num_pages;
+  p.max_kv_len = batch->max_kv_len;
+  p.o_dtype = desc->o_dtype;
+  p.pairs = mla_pairs();
+  p.max_chunks = L.max_chunks;
+  const float scale =
+      desc->sm_scale > 0.f ? desc->sm_scale : 1.0f / sqrtf((float)(desc->kv_lora_rank + desc->rope_dim));
+  p.scale_log2 = scale * kLog2e;
+  p.kv_len = batch->kv_len;
+  p.page_indptr = batch->page_indptr;
+  p.page_indices = batch->page_indices;
+  p.o = o;
+  p.lse = lse;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
+  p.req_info = reinterpret_cast<int4*>(ws + L.req_info);
+  p.chunk_list = reinterpret_cast<int2*>(ws + L.chunk_list);
+  p.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  p.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  p.status = dev_status;
+  return launch_mla(p, q, kv_pool, static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+
 int check_kv(const pd_kv_desc* d, const pd_batch* b) {
   if (d == nullptr || b == nullptr) return PD_ERR_INVALID_ARG;
   const int es = elem_size(d->dtype);

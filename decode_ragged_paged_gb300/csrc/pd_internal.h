@@ -125,6 +125,42 @@ int launch_kv_append(const KvCopyParams& p, cudaStream_t stream);
 int launch_kv_pack(const KvCopyParams& p, cudaStream_t stream);
 int launch_kv_unpack(const KvCopyParams& p, cudaStream_t stream);
 
+// -------------------------------------------------------------- MLA decode
+// Workspace (offsets 256-byte aligned):
+//   hdr        int32[64]   hdr[0] = chunks listed, hdr[1] = chunk length
+//   req_info   int4[B]     {first chunk, chunks, kv_len or -1 if invalid, 0}
+//   chunk_list int2[max_chunks]  (request, chunk) longest first
+//   part_lse   float[max_chunks][Hq]        log2-sum-exp2 of scaled scores
+//   part_o     float[max_chunks][Hq][512]   normalised partial outputs
+struct MlaParams {
+  int32_t batch, hq, page_size, num_pages, max_kv_len, o_dtype, pairs, max_chunks;
+  float scale_log2;  // softmax scale times log2(e)
+  const int32_t* kv_len;
+  const int32_t* page_indptr;
+  const int32_t* page_indices;
+  void* o;
+  float* lse;
+  int32_t* hdr;
+  int4* req_info;
+  int2* chunk_list;
+  float* part_lse;
+  float* part_o;
+  int32_t* status;
+};
+
+struct MlaLayout {
+  size_t hdr, req_info, chunk_list, part_lse, part_o, total;
+  int32_t max_chunks;
+};
+
+// What the MLA kernel supports (latent 512 + rope 64, bf16, 1..128 heads,
+// page size a power of two in [16, 256]); returns a pd_status.
+int mla_supported(int32_t d_c, int32_t d_r, int32_t dtype, int32_t hq, int32_t page_size);
+// CTA pairs of the persistent MLA grid (one CTA per SM).
+int mla_pairs();
+MlaLayout mla_layout(int32_t batch, int32_t hq);
+int launch_mla(MlaParams& p, const void* q, const void* kv_pool, cudaStream_t stream);
+
 // ------------------------------------------------------------ tensor maps
 bool make_pool_map(CUtensorMap* map, const void* pool, int32_t dtype, int32_t num_pages, int32_t hkv,
                    int32_t page_size, int32_t head_dim, int32_t box_cols, int32_t box_rows, bool swizzle128,

@@ -222,6 +222,44 @@ PD_API int pd_attn_mixed(const pd_attn_desc *desc, const pd_batch *batch, const 
                   void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * MLA decode (section "Disaggregated Deployments", "DeepSeek-R1": multi-head
+ * latent attention compresses the KV heads of a token into one latent vector
+ * that every query head reads, so the cache holds one row per token and is
+ * never split by head). With the up-projections folded into q and o (MLA's
+ * published decode form), token j's stored row is
+ * c_j = [c_j^kv (kv_lora_rank values) | k_j^rope (rope_dim values)] and, for
+ * request r and query head h:
+ *   s_j = sm_scale * <q[r][h], c_j>                 (all kv_lora_rank + rope_dim values)
+ *   o[r][h] = sum_j softmax(s)_j * c_j^kv           (the first kv_lora_rank values)
+ *   lse[r][h] = log sum_j exp(s_j)                  (natural log; -inf when kv_len = 0)
+ * Layouts (row-major, device, 16-byte aligned):
+ *   q        [batch][num_qo_heads][kv_lora_rank + rope_dim]
+ *   kv_pool  [num_pages][page_size][kv_lora_rank + rope_dim]   one row per token
+ *   o        [batch][num_qo_heads][kv_lora_rank] (o_dtype); lse fp32 [batch][num_qo_heads] or NULL
+ * One query row per request (row r = request r; the batch's qo_indptr is
+ * ignored); kv_len, page_indptr and page_indices as for attention. Supported:
+ * kv_lora_rank 512, rope_dim 64, bf16 q and pool, 1..128 query heads, page_size
+ * a power of two in [16, 256]; otherwise PD_ERR_UNSUPPORTED. Invalid requests
+ * are skipped and reported through dev_status as for attention.
+ */
+typedef struct {
+  int32_t num_qo_heads; /* Hq: query heads reading the latent row, 1..128 */
+  int32_t kv_lora_rank; /* latent (value) width: 512 */
+  int32_t rope_dim;     /* rope width, scores only: 64 */
+  int32_t page_size;    /* tokens per page */
+  int32_t kv_dtype;     /* pd_dtype of q and kv_pool: PD_BF16 */
+  int32_t o_dtype;      /* pd_dtype of o */
+  float sm_scale;       /* softmax scale; <= 0 selects 1/sqrt(kv_lora_rank + rope_dim) */
+} pd_mla_desc;
+
+/* Bytes of device workspace pd_mla_decode needs (0 for an invalid descriptor). */
+PD_API size_t pd_mla_workspace_size(const pd_mla_desc *desc, const pd_batch *batch);
+
+PD_API int pd_mla_decode(const pd_mla_desc *desc, const pd_batch *batch, const void *q, const void *kv_pool,
+                         void *o, float *lse, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                         void *stream);
+
+/*
  * KV append (section "KV Messenger": page copies of a layer start once the
  * model has appended that layer's KV entries). The batch's qo_indptr counts
  * the new tokens: request r brings n_r = qo_indptr[r+1] - qo_indptr[r] rows of

@@ -164,3 +164,43 @@ def test_layer_range_outside_the_pool_is_rejected(lib):
     for l0, n in [(-1, 1), (0, 0), (2, 2), (3, 1)]:
         assert lib.pd_kv_pack_layers(ctypes.byref(d), ctypes.byref(b), l0, n, 16, 16, 16, 1 << 20, 16, None,
                                      None) == pd.PD_ERR_INVALID_ARG
+
+
+def _mla_desc(**kw):
+    d = dict(num_qo_heads=128, kv_lora_rank=512, rope_dim=64, page_size=64, kv_dtype=pd.PD_BF16,
+             o_dtype=pd.PD_BF16, sm_scale=0.0)
+    d.update(kw)
+    return pd.MlaDesc(**d)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_qo_heads=0), pd.PD_ERR_INVALID_ARG),
+    (dict(num_qo_heads=129), pd.PD_ERR_UNSUPPORTED),     # more heads than one 128-row tile
+    (dict(kv_lora_rank=256), pd.PD_ERR_UNSUPPORTED),
+    (dict(rope_dim=32), pd.PD_ERR_UNSUPPORTED),
+    (dict(kv_dtype=pd.PD_F32), pd.PD_ERR_UNSUPPORTED),
+    (dict(page_size=8), pd.PD_ERR_UNSUPPORTED),
+    (dict(page_size=48), pd.PD_ERR_UNSUPPORTED),
+    (dict(o_dtype=9), pd.PD_ERR_INVALID_ARG),
+])
+def test_mla_rejects_bad_descriptor(lib, kw, code):
+    rc = lib.pd_mla_decode(ctypes.byref(_mla_desc(**kw)), ctypes.byref(_batch()), 16, 16, 16, 16, 16, 1 << 30,
+                           None, None)
+    assert rc == code
+    assert lib.pd_mla_workspace_size(ctypes.byref(_mla_desc(**kw)), ctypes.byref(_batch())) == 0
+
+
+def test_mla_workspace_and_pointer_checks(lib):
+    d, b = _mla_desc(), _batch()
+    n = lib.pd_mla_workspace_size(ctypes.byref(d), ctypes.byref(b))
+    assert n > 0 and n % 256 == 0
+    # partial outputs for batch + one chunk per SM at most: grows with the batch
+    assert lib.pd_mla_workspace_size(ctypes.byref(d), ctypes.byref(_batch(batch_size=20))) > n
+    assert lib.pd_mla_decode(ctypes.byref(d), ctypes.byref(b), 16, 16, 16, 16, 16, n - 1, None,
+                             None) == pd.PD_ERR_WORKSPACE
+    assert lib.pd_mla_decode(ctypes.byref(d), ctypes.byref(b), 24, 16, 16, 16, 16, n, None,
+                             None) == pd.PD_ERR_INVALID_ARG                                   # misaligned q
+    assert lib.pd_mla_decode(ctypes.byref(d), ctypes.byref(_batch(kv_len=None)), 16, 16, 16, 16, 16, n, None,
+                             None) == pd.PD_ERR_INVALID_ARG
+    assert lib.pd_mla_decode(ctypes.byref(d), ctypes.byref(_batch(batch_size=0)), None, None, None, None, None, 0,
+                             None, None) == pd.PD_OK
