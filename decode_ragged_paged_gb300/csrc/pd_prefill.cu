@@ -9,10 +9,10 @@
 //
 // One persistent CTA per SM walks a list of (request, 128-row q tile, query
 // head) items, heaviest first. Warp roles:
-//   warp 0    TMA producer of Q tiles (double buffered) and K tiles (2-slot
-//             ring), each tile one 128-byte-swizzled box per page and 64-column
-//             half; boxes past the request's pages are fetched out of range
-//             and arrive as zeros;
+//   warp 0    TMA producer of Q tiles (a ring of two or three) and K tiles (a
+//             ring of three or two), each tile one 128-byte-swizzled box per
+//             page and 64-column half; boxes past the request's pages are
+//             fetched out of range and arrive as zeros;
 //   warp 6    TMA producer of V tiles (2-slot ring), same boxes;
 //   warp 1    allocates 512 TMEM columns and issues S = Q K^T (tcgen05.mma)
 //             into one of two S buffers;
@@ -25,7 +25,7 @@
 //             only when the running max grows by more than 2^8; an item's
 //             epilogue (O / l, log-sum-exp) runs after the next item's first
 //             tile, a full bf16 O tile staged in the item's Q buffer and
-//             stored by TMA.
+//             stored by TMA, other tiles stored row by row.
 // Every wait is bounded; on a timeout the CTA records PD_DEV_TIMEOUT, drains
 // and frees its TMEM.
 #include <math.h>
@@ -56,35 +56,29 @@ static_assert((kSB + 2) * 128 <= 512, "TMEM columns");
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 constexpr int kBuckets = 1024;
 
-// shared-memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t kOffQ = 0;                  // 2 tiles
-// K and V ring depths (five tiles between them; a full bf16 O tile is staged
-// in its item's Q buffer)
-#ifndef PD_PREFILL_K_SLOTS
-#define PD_PREFILL_K_SLOTS 3
-#endif
-#ifndef PD_PREFILL_V_SLOTS
-#define PD_PREFILL_V_SLOTS (5 - PD_PREFILL_K_SLOTS)
-#endif
-constexpr int kKSlots = PD_PREFILL_K_SLOTS;
-constexpr int kVSlots = PD_PREFILL_V_SLOTS;
-static_assert(kKSlots >= 2 && kVSlots >= 2 && kKSlots + kVSlots <= 5, "ring depths");
-// A V slot is freed by the pv_done phase of its previous tile. A waiter on that
-// barrier must never fall two phases behind, which holds while the ring is no
-// deeper than the S buffers (K slots have their own k_empty barriers).
-static_assert(kVSlots <= kSB, "V ring deeper than the S buffers");
-constexpr uint32_t kOffK = 2 * kTileBytes;
-constexpr uint32_t kOffV = (2 + kKSlots) * kTileBytes;
-constexpr uint32_t kOffBar = 7 * kTileBytes;
-constexpr size_t kPrefillSmem = 7 * kTileBytes + 256 + 1024;
+// Shared memory (offsets from a 1024-byte aligned base): QB Q buffers, then a
+// ring of KS K slots and one of 7 - QB - KS V slots, seven 32 KiB tiles in all.
+// Two shapes are built: QB 3 / KS 2 for calls made mostly of long query blocks
+// (a Q tile is fetched an item ahead; full bf16 O tiles are staged in their Q
+// buffer and written by TMA), QB 2 / KS 3 for decode-like calls (K runs a tile
+// further ahead; O rows are stored directly, so a Q buffer is free once its
+// item's last S product is done).
+constexpr uint32_t kOffQ = 0;
+constexpr int kRingTiles = 7;
+constexpr uint32_t kOffBar = kRingTiles * kTileBytes;
+constexpr size_t kPrefillSmem = kRingTiles * kTileBytes + 256 + 1024;
 
-struct Bars {
-  uint64_t q_full[2], q_empty[2], k_full[kKSlots], k_empty[kKSlots], v_full[kVSlots];
+// Every ring slot has its own full and empty barriers: a slot freed by the
+// phases of a barrier that serves other buffers could see its waiter fall two
+// phases behind, where a parity wait no longer tells them apart.
+template <int QB, int KS, int VS>
+struct BarsT {
+  uint64_t q_full[QB], q_empty[QB], k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
   uint64_t s_full[kSB], p_full[kSB], pv_done[kSB], drain, o_sync;
   uint32_t tmem_slot;
   int abort;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(BarsT<3, 2, 2>) <= 256 && sizeof(BarsT<2, 3, 2>) <= 256, "barrier block");
 
 // An item is (request, q tile of p.tile_rows query rows, group of p.tile_heads
 // query heads sharing KV head g). Tile row m holds query row q0 + m / tile_heads
@@ -121,6 +115,15 @@ __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int it) {
   I.pbase = p.page_indptr[I.r];
   I.need = (I.kv + p.page_size - 1) / p.page_size;
   return I;
+}
+
+// With staging on, a full bf16 O tile is staged in its item's Q buffer and
+// stored by TMA, which then frees that buffer; other tiles are stored row by
+// row, and their Q buffer is free as soon as the item's last S product has
+// completed.
+template <bool STAGE>
+__device__ __forceinline__ bool o_staged(const PrefillParams& p, const PItem& I) {
+  return STAGE && p.o_dtype == PD_BF16 && I.rows == p.tile_rows;
 }
 
 // The item after the current one is read while the current one is worked on,
@@ -247,10 +250,16 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
 }
 
 // ----------------------------------------------------------------- kernel
+template <int QB, int KS, bool STAGE>
 __global__ void __launch_bounds__(kThreadsPf, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                    const PrefillParams p) {
+  constexpr int kQB = QB, kKSlots = KS, kVSlots = kRingTiles - QB - KS;
+  static_assert(kQB >= 2 && kKSlots >= 2 && kVSlots >= 2, "ring depths");
+  constexpr uint32_t kOffK = kQB * kTileBytes;
+  constexpr uint32_t kOffV = (kQB + kKSlots) * kTileBytes;
+  using Bars = BarsT<kQB, kKSlots, kVSlots>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base + kOffQ;
@@ -261,16 +270,19 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kQB; ++i) {
       mbar_init(&bars->q_full[i], 1);
-      // the item's last S product, and the read of the O tile staged in it
-      mbar_init(&bars->q_empty[i], 2);
+      // the item's last S product, or the read of the O tile staged in it
+      mbar_init(&bars->q_empty[i], 1);
     }
     for (int i = 0; i < kKSlots; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
     }
-    for (int i = 0; i < kVSlots; ++i) mbar_init(&bars->v_full[i], 1);
+    for (int i = 0; i < kVSlots; ++i) {
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
     for (int i = 0; i < kSB; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 4);
@@ -309,8 +321,8 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       const PItem I = nxt;
       nxt = prefill_item_or_empty(p, it + gridDim.x, n_items);
       if (!is_v) {
-        const int qb = it_ctr & 1;
-        if (!warp_mbar_wait(&bars->q_empty[qb], ((it_ctr >> 1) & 1u) ^ 1u, abort, p.status)) break;
+        const int qb = it_ctr % kQB;
+        if (!warp_mbar_wait(&bars->q_empty[qb], ((it_ctr / kQB) & 1u) ^ 1u, abort, p.status)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars->q_full[qb], kTileBytes);
           tma_load_3d(sQ + qb * kTileBytes, &tm_q, 0, I.h, I.q0, &bars->q_full[qb]);
@@ -325,13 +337,9 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         const TileBox box = tile_box(p, I.pbase, I.need, j, lane);  // page ids read before the slot wait
         // A K slot is free again once the S product of its previous tile has
         // completed (k_empty); a V slot once the P V product of its previous
-        // tile u = kv_ctr - depth has (pv_done, waited for every tile in order).
-        if (!is_v) {
-          ok = warp_mbar_wait(&bars->k_empty[slot], ((kv_ctr / kKSlots) & 1u) ^ 1u, abort, p.status);
-        } else if (kv_ctr >= depth) {
-          const uint32_t u = kv_ctr - depth;
-          ok = warp_mbar_wait(&bars->pv_done[u % kSB], (u / kSB) & 1u, abort, p.status);
-        }
+        // tile has (v_empty).
+        ok = is_v ? warp_mbar_wait(&bars->v_empty[slot], ((kv_ctr / kVSlots) & 1u) ^ 1u, abort, p.status)
+                  : warp_mbar_wait(&bars->k_empty[slot], ((kv_ctr / kKSlots) & 1u) ^ 1u, abort, p.status);
         if (ok) {
           if (!is_v)
             load_kv_tile(p, box, &tm_k, I.g, sK + slot * kTileBytes, &bars->k_full[slot], lane);
@@ -354,8 +362,8 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++it_ctr) {
       const PItem I = nxt;
       nxt = prefill_item_or_empty(p, it + gridDim.x, n_items);
-      const int qb = it_ctr & 1;
-      ok = warp_mbar_wait(&bars->q_full[qb], (it_ctr >> 1) & 1u, abort, p.status);
+      const int qb = it_ctr % kQB;
+      ok = warp_mbar_wait(&bars->q_full[qb], (it_ctr / kQB) & 1u, abort, p.status);
       if (!ok) break;
       tc_fence_after();
       const uint64_t dq = sw128_desc(sQa + qb * kTileBytes, 16, 1024);
@@ -377,12 +385,12 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
           }
           tc_commit(&bars->s_full[sb]);
           tc_commit(&bars->k_empty[slot]);
-          if (j == I.n_kv - 1) tc_commit(&bars->q_empty[qb]);
+          if (j == I.n_kv - 1 && !o_staged<STAGE>(p, I)) tc_commit(&bars->q_empty[qb]);
         }
         __syncwarp();
       }
       if (!ok) break;
-      if (I.n_kv == 0 && lane == 0) mbar_arrive(&bars->q_empty[qb]);
+      if (I.n_kv == 0 && !o_staged<STAGE>(p, I) && lane == 0) mbar_arrive(&bars->q_empty[qb]);
       __syncwarp();
     }
     // all MMAs of this thread complete before TMEM is released
@@ -433,7 +441,8 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
           for (int kk = 0; kk < kBN / 16; ++kk)
             tc_mma_f16_tmem_a(t_o, pa + 8 * kk, desc_advance(dv, kk * 2048), idesc_pv,
                               (j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&bars->pv_done[sb]);  // also frees the V slot and the S buffer
+          tc_commit(&bars->pv_done[sb]);  // also frees the S buffer
+          tc_commit(&bars->v_empty[slot]);
         }
         __syncwarp();
       }
@@ -460,6 +469,7 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
     bool ok = true;
     struct Pend {
       int q0, h, rows, n_kv, qb, ob;  // h: the tile's first query head; rows: valid query rows
+      bool staged;  // O goes through the Q buffer (which it then releases)
       uint32_t last;  // running index of the item's last tile
       float m, l;
     };
@@ -495,7 +505,7 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
 #pragma unroll
         for (int e = 0; e < kD; ++e) v[e] = 0u;
       }
-      const bool staged = p.o_dtype == PD_BF16 && E.rows == p.tile_rows;
+      const bool staged = E.staged;
       if (staged) {
         // full tile: stage bf16 O (128-byte swizzled like Q) in the item's Q
         // buffer, free now that its last S product has completed, and write it
@@ -546,7 +556,6 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       if (store && p.lse != nullptr)
         p.lse[(int64_t)(E.q0 + qrow) * p.hq + E.h + qhead] =
             (E.n_kv > 0 && E.l > 0.f) ? (E.m + log2f(E.l)) * kLn2 : -INFINITY;
-      if (o_issuer && !staged) mbar_arrive(&bars->q_empty[E.qb]);  // nothing staged in this Q buffer
       tc_fence_before();
       return true;
     };
@@ -554,7 +563,7 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++it_ctr) {
       const PItem I = nxt;
       nxt = prefill_item_or_empty(p, it + gridDim.x, n_items);
-      const int qb = it_ctr & 1, ob = it_ctr & 1;
+      const int qb = it_ctr % kQB, ob = it_ctr & 1;
       const uint32_t o_addr = t_lane + col_o(ob);
       const int lim = I.kv - I.qo_len + I.qt * p.tile_rows + qrow;  // last key this row may see (causal)
       // l: sum of the weights (normalises O, gives the lse); P enters P V
@@ -655,7 +664,7 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       }
       if (!ok) break;
       release_staged();
-      const Pend cur{I.q0, I.h, I.rows, I.n_kv, qb, ob, s_ctr - 1, m, l};
+      const Pend cur{I.q0, I.h, I.rows, I.n_kv, qb, ob, o_staged<STAGE>(p, I), s_ctr - 1, m, l};
       if (I.n_kv == 0) {
         // no tile to overlap with: finish the pending item and this one now
         if (has_pend) {
@@ -731,14 +740,18 @@ int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const vo
       !make_pool_map(&tk, k_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true, p.nhd != 0) ||
       !make_pool_map(&tv, v_pool, PD_BF16, p.num_pages, p.hkv, p.page_size, kD, 64, pb, true, p.nhd != 0))
     return PD_ERR_CUDA;
-  static int configured_device = -1;
+  // Calls whose requests average at least half a tile of query rows run the
+  // shape that fetches Q an item ahead and stages O; decode-like calls the
+  // deeper K ring and direct O stores.
+  const bool long_q = (int64_t)p.total_qo * 2 >= (int64_t)kBM * p.batch;
+  auto kernel = long_q ? prefill_kernel<3, 2, true> : prefill_kernel<2, 3, false>;
+  static int configured_device[2] = {-1, -1};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;
-  if (configured_device != dev) {
-    if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrefillSmem) !=
-        cudaSuccess)
+  if (configured_device[long_q] != dev) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrefillSmem) != cudaSuccess)
       return PD_ERR_CUDA;
-    configured_device = dev;
+    configured_device[long_q] = dev;
   }
   last_kernel() = "prefill_kernel";
   prefill_plan_kernel<<<1, 1024, 0, stream>>>(p);
@@ -759,7 +772,7 @@ int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const vo
   cfg.attrs = attr;
   cfg.numAttrs = profile_events().start != nullptr ? 0 : 1;
   profile_begin(stream);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_kernel, tq, tk, tv, to, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, to, p);
   profile_end(stream);
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
 }
