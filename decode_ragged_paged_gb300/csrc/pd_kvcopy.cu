@@ -131,63 +131,79 @@ __device__ __forceinline__ Unit unit_of(int64_t u, int kp, int hkv, int layers, 
 }  // namespace
 
 // --------------------------------------------------------------- append
-// One CTA per new-token row at a time: all heads of K and V of that row.
-__global__ void __launch_bounds__(kCopyThreads) kv_append_kernel(const KvCopyParams p) {
-  const int row_bytes = p.head_dim * p.elem_size;
-  const int vpr = row_bytes / 16;               // vectors per (token, head) row
-  const int per_row = 2 * p.hkv * vpr;          // vectors of K and V of one token
-  const int total_rows = p.max_new;             // rows of k_new / v_new
-  for (int row = blockIdx.x; row < total_rows; row += gridDim.x) {
-    // request owning the row: last r with new_indptr[r] <= row
-    int lo = 0, hi = p.batch;  // answer in [lo, hi)
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(p.new_indptr + mid) <= row) lo = mid;
-      else hi = mid;
+// Each CTA takes blocks of up to kAppendRows consecutive new-token rows. One
+// thread per row finds the row's request (binary search over the new-token
+// indptr), checks it and looks up its page, all rows at once; then the CTA
+// copies the block's K and V rows (every head) with several 16-byte vectors in
+// flight per thread.
+constexpr int kAppendRows = 32;
+
+__global__ void __launch_bounds__(kCopyThreads) kv_append_kernel(const KvCopyParams p, int rows_per_cta) {
+  __shared__ int s_page[kAppendRows], s_slot[kAppendRows];
+  const int vpr = p.head_dim * p.elem_size / 16;  // vectors per (token, head) row
+  const int hv = p.hkv * vpr;                     // vectors of one token's K (or V)
+  const int per_row = 2 * hv;                     // vectors of K and V of one token
+  for (int r0 = blockIdx.x * rows_per_cta; r0 < p.max_new; r0 += gridDim.x * rows_per_cta) {
+    const int nrows = min(rows_per_cta, p.max_new - r0);
+    if (threadIdx.x < nrows) {
+      const int row = r0 + threadIdx.x;
+      // request owning the row: last r with new_indptr[r] <= row
+      int lo = 0, hi = p.batch;  // answer in [lo, hi)
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(p.new_indptr + mid) <= row) lo = mid;
+        else hi = mid;
+      }
+      const int r = lo;
+      const int a = __ldg(p.new_indptr + r), b = __ldg(p.new_indptr + r + 1);
+      int page = -1, slot = 0;
+      if (row >= a && row < b) {  // else: a row past the last request's tokens
+        const int n_new = b - a, n = __ldg(p.kv_len + r);
+        const int pa = __ldg(p.page_indptr + r), pb = __ldg(p.page_indptr + r + 1);
+        const int t = n - n_new + (row - a);
+        if (n_new <= n && n <= p.max_kv_len && pa >= 0 && pb >= pa && (int64_t)(pb - pa) * p.page_size >= n) {
+          const int pg = __ldg(p.page_indices + pa + t / p.page_size);
+          if (pg >= 0 && pg < p.num_pages) {
+            page = pg;
+            slot = t % p.page_size;
+          } else {
+            report(p.status, PD_DEV_BAD_PAGE_TABLE);
+          }
+        } else {
+          report(p.status, PD_DEV_BAD_LENGTH);
+        }
+      }
+      s_page[threadIdx.x] = page;
+      s_slot[threadIdx.x] = slot;
     }
-    const int r = lo;
-    const int a = __ldg(p.new_indptr + r), b = __ldg(p.new_indptr + r + 1);
-    if (row < a || row >= b) continue;  // row past the last request's tokens
-    const int n_new = b - a, n = __ldg(p.kv_len + r);
-    const int pa = __ldg(p.page_indptr + r), pb = __ldg(p.page_indptr + r + 1);
-    const int t = n - n_new + (row - a);
-    bool ok = n_new <= n && n <= p.max_kv_len && pa >= 0 && pb >= pa &&
-              (int64_t)(pb - pa) * p.page_size >= n;
-    int32_t page = 0;
-    if (ok) {
-      page = __ldg(p.page_indices + pa + t / p.page_size);
-      ok = page >= 0 && page < p.num_pages;
-      if (!ok && threadIdx.x == 0) report(p.status, PD_DEV_BAD_PAGE_TABLE);
-    } else if (threadIdx.x == 0) {
-      report(p.status, PD_DEV_BAD_LENGTH);
-    }
-    if (!ok) continue;
-    const int slot = t % p.page_size;
-    uint4 tmp[kUnroll];
-    // Every thread loads its vectors first, then stores them.
-    for (int base = 0; base < per_row; base += kCopyThreads * kUnroll) {
+    __syncthreads();
+    const int nvec = nrows * per_row;
+    for (int base = 0; base < nvec; base += kCopyThreads * kUnroll) {
+      uint4 tmp[kUnroll];
+      // Every thread loads its vectors first, then stores them.
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int i = base + u * kCopyThreads + threadIdx.x;
-        if (i < per_row) {
-          const int kv = i / (p.hkv * vpr);
-          const int rem = i - kv * p.hkv * vpr;
-          const uint4* src = static_cast<const uint4*>(kv ? p.src2 : p.src) + (int64_t)row * p.hkv * vpr + rem;
-          tmp[u] = ld_stream(src);
+        if (i < nvec) {
+          const int k = i / per_row, rem = i - k * per_row;
+          const int kv = rem >= hv, w = rem - kv * hv;
+          if (s_page[k] >= 0)
+            tmp[u] = ld_stream(static_cast<const uint4*>(kv ? p.src2 : p.src) + (int64_t)(r0 + k) * hv + w);
         }
       }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int i = base + u * kCopyThreads + threadIdx.x;
-        if (i < per_row) {
-          const int kv = i / (p.hkv * vpr);
-          const int rem = i - kv * p.hkv * vpr;
-          const int h = rem / vpr, v = rem - h * vpr;
-          uint4* dst = static_cast<uint4*>(kv ? p.dst2 : p.dst) + pool_vec(p, page, h, slot, vpr) + v;
-          *dst = tmp[u];
+        if (i < nvec) {
+          const int k = i / per_row, rem = i - k * per_row;
+          const int kv = rem >= hv, w = rem - kv * hv;
+          const int h = w / vpr, v = w - h * vpr;
+          if (s_page[k] >= 0)
+            static_cast<uint4*>(kv ? p.dst2 : p.dst)[pool_vec(p, s_page[k], h, s_slot[k], vpr) + v] = tmp[u];
         }
       }
     }
+    __syncthreads();  // the block's metadata is rewritten next
   }
 }
 
@@ -267,11 +283,16 @@ int copy_grid() { return device_sm_count() * (2048 / kCopyThreads); }
 
 int launch_kv_append(const KvCopyParams& p, cudaStream_t stream) {
   if (p.max_new <= 0 || p.batch <= 0) return PD_OK;
-  int grid = copy_grid();
-  if (grid > p.max_new) grid = p.max_new;
+  // blocks of consecutive rows, about one per CTA slot of the GPU
+  const int slots = copy_grid();
+  int rows_per_cta = (p.max_new + slots - 1) / slots;
+  if (rows_per_cta > kAppendRows) rows_per_cta = kAppendRows;
+  const int grid = (p.max_new + rows_per_cta - 1) / rows_per_cta < slots
+                       ? (p.max_new + rows_per_cta - 1) / rows_per_cta
+                       : slots;
   last_kernel() = "kv_append_kernel";
   profile_begin(stream);
-  kv_append_kernel<<<grid, kCopyThreads, 0, stream>>>(p);
+  kv_append_kernel<<<grid, kCopyThreads, 0, stream>>>(p, rows_per_cta);
   profile_end(stream);
   return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
 }
