@@ -8,7 +8,8 @@
 // tokens, so row i may attend keys j <= kv_len - qo_len + i.
 //
 // One persistent CTA per SM walks a list of (request, 128-row q tile, query
-// head) items, heaviest first. Warp roles:
+// head) items sorted heaviest first, in serpentine order (round k forward over
+// the grid, round k + 1 backward). Warp roles:
 //   warp 0    TMA producer of Q tiles (a ring of two or three) and K tiles (a
 //             ring of three or two), each tile one 128-byte-swizzled box per
 //             page and 64-column half; boxes past the request's pages are
@@ -124,6 +125,13 @@ __device__ __forceinline__ PItem prefill_item(const PrefillParams& p, int it) {
 template <bool STAGE>
 __device__ __forceinline__ bool o_staged(const PrefillParams& p, const PItem& I) {
   return STAGE && p.o_dtype == PD_BF16 && I.rows == p.tile_rows;
+}
+
+// Item a CTA takes in round k: rounds alternate direction over the grid, so on
+// a list sorted heaviest first every CTA's total stays near the mean.
+__device__ __forceinline__ int round_item(uint32_t k) {
+  const int g = (int)gridDim.x, b = (int)blockIdx.x;
+  return (int)k * g + ((k & 1u) ? g - 1 - b : b);
 }
 
 // The item after the current one is read while the current one is worked on,
@@ -316,10 +324,10 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
     // double the rate at which a tile's page boxes are requested.
     const bool is_v = warp == kWarpV;
     uint32_t it_ctr = 0, kv_ctr = 0;
-    PItem nxt = prefill_item_or_empty(p, blockIdx.x, n_items);
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++it_ctr) {
+    PItem nxt = prefill_item_or_empty(p, round_item(0), n_items);
+    for (int it = round_item(0); it < n_items; ++it_ctr, it = round_item(it_ctr)) {
       const PItem I = nxt;
-      nxt = prefill_item_or_empty(p, it + gridDim.x, n_items);
+      nxt = prefill_item_or_empty(p, round_item(it_ctr + 1), n_items);
       if (!is_v) {
         const int qb = it_ctr % kQB;
         if (!warp_mbar_wait(&bars->q_empty[qb], ((it_ctr / kQB) & 1u) ^ 1u, abort, p.status)) break;
@@ -358,10 +366,10 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
     const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK);
     uint32_t it_ctr = 0, kv_ctr = 0;
     bool ok = true;
-    PItem nxt = prefill_item_or_empty(p, blockIdx.x, n_items);
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++it_ctr) {
+    PItem nxt = prefill_item_or_empty(p, round_item(0), n_items);
+    for (int it = round_item(0); it < n_items && ok; ++it_ctr, it = round_item(it_ctr)) {
       const PItem I = nxt;
-      nxt = prefill_item_or_empty(p, it + gridDim.x, n_items);
+      nxt = prefill_item_or_empty(p, round_item(it_ctr + 1), n_items);
       const int qb = it_ctr % kQB;
       ok = warp_mbar_wait(&bars->q_full[qb], (it_ctr / kQB) & 1u, abort, p.status);
       if (!ok) break;
@@ -407,10 +415,10 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
     const uint32_t sVa = smem_u32(sV);
     uint32_t kv_ctr = 0, it_ctr = 0;
     bool ok = true;
-    PItem nxt = prefill_item_or_empty(p, blockIdx.x, n_items);
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++it_ctr) {
+    PItem nxt = prefill_item_or_empty(p, round_item(0), n_items);
+    for (int it = round_item(0); it < n_items && ok; ++it_ctr, it = round_item(it_ctr)) {
       const PItem I = nxt;
-      nxt = prefill_item_or_empty(p, it + gridDim.x, n_items);
+      nxt = prefill_item_or_empty(p, round_item(it_ctr + 1), n_items);
       const uint32_t t_o = tmem + col_o(it_ctr & 1);  // this item's O accumulator
       for (int j = 0; j < I.n_kv; ++j, ++kv_ctr) {
         const int slot = kv_ctr % kVSlots;
@@ -559,10 +567,10 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       tc_fence_before();
       return true;
     };
-    PItem nxt = prefill_item_or_empty(p, blockIdx.x, n_items);
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++it_ctr) {
+    PItem nxt = prefill_item_or_empty(p, round_item(0), n_items);
+    for (int it = round_item(0); it < n_items && ok; ++it_ctr, it = round_item(it_ctr)) {
       const PItem I = nxt;
-      nxt = prefill_item_or_empty(p, it + gridDim.x, n_items);
+      nxt = prefill_item_or_empty(p, round_item(it_ctr + 1), n_items);
       const int qb = it_ctr % kQB, ob = it_ctr & 1;
       const uint32_t o_addr = t_lane + col_o(ob);
       const int lim = I.kv - I.qo_len + I.qt * p.tile_rows + qrow;  // last key this row may see (causal)
