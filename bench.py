@@ -537,6 +537,30 @@ def measure_rows(args, dev, peaks) -> dict:
                           "frac_hbm": round(nbytes / kms / 1e6 / hbm, 4), "bound": "hbm", "bytes": nbytes}
     del w, wsn
 
+    # MLA decode over a paged latent cache: 128 heads read one 576-value row per
+    # token (scores over all of it, values its first 512)
+    w = torch_gen.mla_decode_batch(device=dev)
+    toks = int(w["kv_len_host"].sum())
+    b_, h_, dc, dr = len(w["kv_len_host"]), w["heads"], w["d_c"], w["d_r"]
+    mbytes = toks * (dc + dr) * 2 + w["q"].numel() * 2 + b_ * h_ * dc * 2 + b_ * h_ * 4
+    mflops = 2 * toks * h_ * ((dc + dr) + dc)
+    try:
+        o = torch.empty((b_, h_, dc), dtype=torch.bfloat16, device=dev)
+        ms, kms, hus = timed(lambda: pd.pd_mla_decode(w["q"], w["kv_pool"], w["kv_len"], w["page_indptr"],
+                                                      w["page_indices"], kv_lora_rank=dc, sm_scale=192 ** -0.5,
+                                                      max_kv_len=4096, o=o), reps, warm, flush)
+        t = mflops / (kms * 1e-3) / 1e12
+        rows["mla_decode"] = {"workload": "MLA decode: 128 requests, kv_len U[512,4096], 128 heads, latent 512 + "
+                                          "rope 64, page 64, bf16",
+                              "kernel": pd.pd_last_kernel(), "ms": round(ms, 5), "kernel_ms": round(kms, 5),
+                              "host_us": round(hus, 1), "GBs": round(mbytes / kms / 1e6, 1),
+                              "frac_hbm": round(mbytes / kms / 1e6 / hbm, 4), "TFLOPs": round(t, 1),
+                              "frac_bf16": round(t / peaks["bf16"], 4),
+                              "bound": "hbm (about 220 flop/B, below the ridge)", "bytes": mbytes, "flops": mflops}
+    except pd.PdError as e:
+        rows["mla_decode"] = {"status": str(e)}
+    del w
+
     w = torch_gen.kv_handoff(device=dev)
     byts = 2 * w["buffer"].numel()
     ms, kms, hus = timed(lambda: pd.pd_kv_pack(w["k_src"], w["v_src"], w["kv_len"], w["src_indptr"], w["src_indices"],
@@ -690,6 +714,10 @@ def profile_row(name: str, reps: int) -> None:
         w = torch_gen.mixed_1p_nd()
         fn = lambda: pd.pd_attn_mixed(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
                                       w["page_indices"], w["qo_indptr"], max_qo_len=1024, max_kv_len=1024)
+    elif name == "mla_decode":
+        w = torch_gen.mla_decode_batch()
+        fn = lambda: pd.pd_mla_decode(w["q"], w["kv_pool"], w["kv_len"], w["page_indptr"], w["page_indices"],
+                                      kv_lora_rank=w["d_c"], sm_scale=192 ** -0.5, max_kv_len=4096)
     elif name in ("pack", "unpack"):
         w = torch_gen.kv_handoff()
         if name == "pack":
@@ -716,7 +744,8 @@ def main():
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile-row", default=None,
-                    help="run only this row's call (decode, decode_mha, append, prefill, mixed, pack, unpack) for ncu")
+                    help="run only this row's call (decode, decode_mha, append, prefill, mixed, mla_decode, pack, "
+                         "unpack) for ncu")
     ap.add_argument("--profile-reps", type=int, default=3)
     args = ap.parse_args()
     if args.profile_row:

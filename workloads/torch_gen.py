@@ -96,3 +96,20 @@ def kv_handoff(seed: int = 5, batch: int = 8, length: int = 512, layers: int = 4
         buffer=torch.empty(per * batch, dtype=torch.uint8, device=device),
         kv_len_host=kv, layers=layers, heads=heads, head_dim=head_dim,
     )
+
+
+def mla_decode_batch(seed: int = 7, batch: int = 128, kv_lo: int = 512, kv_hi: int = 4096, heads: int = 128,
+                     d_c: int = 512, d_r: int = 64, page: int = 64, device="cuda") -> dict:
+    """MLA decode: 128 requests, kv_len U[512, 4096], 128 query heads over one
+    512 + 64 latent row per token, page 64, bf16; pages a seeded permutation."""
+    g = _gen(seed, device)
+    kv = np.random.default_rng(seed + 1000).integers(kv_lo, kv_hi + 1, size=batch)
+    page_indptr, npages = _csr(kv, page, device)
+    return dict(
+        kv_len=torch.from_numpy(kv.astype(np.int32)).to(device),
+        page_indptr=page_indptr,
+        page_indices=torch.randperm(npages, generator=g, device=device, dtype=torch.int32),
+        kv_pool=torch.randn((npages, page, d_c + d_r), generator=g, device=device, dtype=torch.bfloat16),
+        q=torch.randn((batch, heads, d_c + d_r), generator=g, device=device, dtype=torch.bfloat16),
+        kv_len_host=kv, heads=heads, d_c=d_c, d_r=d_r, page=page,
+    )
