@@ -25,9 +25,14 @@
 //                warp 0    TMA producer: the request's Q tile (9 boxes of 64
 //                          columns x 128 heads) and 32-token latent tiles
 //                          (2-slot ring, 9 x 128-byte-swizzled boxes per page);
-//                warp 1    allocates TMEM, issues S = Q C^T (36 MMAs of K 16);
+//                warps 1, 6, 8  issue S = Q C^T as three partial products
+//                          over three column chunks each (12 MMAs of K 16
+//                          apiece: one thread issues a tcgen05.mma about
+//                          every 94 cycles whatever N, so one issuer would
+//                          bound the tile); warp 1 also allocates TMEM;
 //                warp 7    issues O += P C_h with P read from TMEM;
-//                warps 2-5 one head per thread: online softmax (lazy O
+//                warps 2-5 one head per thread: S = the sum of the three
+//                          partials, online softmax (lazy O
 //                          rescale), the epilogue (final o and lse, or a fp32
 //                          partial for a request split into chunks);
 //   3. merge   requests split into chunks: log-sum-exp merge of the partials.
@@ -51,8 +56,13 @@ constexpr int kRows = 128;               // tile rows: query heads, zero-padded
 constexpr int kN = 32;                   // tokens per latent tile
 constexpr int kHalfV = kDc / 2;          // value columns per CTA of a pair
 constexpr int kVChunks = kHalfV / 64;    // 4 column chunks per half
-constexpr int kThreadsMla = 256;
+constexpr int kThreadsMla = 288;         // 9 warps
 constexpr int kWarpPV = 7;
+constexpr int kSIssuers = 3;             // warps issuing the partial score products
+constexpr int kMmaPerIssuer = (kW / 16) / kSIssuers;
+static_assert(kMmaPerIssuer * kSIssuers * 16 == kW && kMmaPerIssuer % 4 == 0, "issuers take whole chunks");
+// index of the partial product warp w issues, or -1
+__device__ __forceinline__ int s_issuer(int w) { return w == 1 ? 0 : w == 6 ? 1 : w == 8 ? 2 : -1; }
 constexpr int kSlots = 2;                // latent tile ring
 constexpr int kSB = 2;                   // S / P buffers in TMEM
 constexpr uint32_t kQChunk = kRows * 128;          // 16 KiB: 128 rows x 64 values
@@ -64,9 +74,10 @@ constexpr uint32_t kOffBar = kQBytes + kSlots * kCBytes;
 constexpr size_t kMlaSmem = kOffBar + 256 + 1024;
 static_assert(kMlaSmem <= 227 * 1024, "shared memory");
 constexpr uint32_t kTmemCols = 512;
-__device__ __forceinline__ uint32_t col_s(int b) { return (uint32_t)b * kN; }
+// partial score product `part` of S buffer b (P is written over part 0)
+__device__ __forceinline__ uint32_t col_s(int b, int part = 0) { return (uint32_t)(b * kSIssuers + part) * kN; }
 constexpr uint32_t kColO = 256;                    // O half: columns [256, 512)
-static_assert(kSB * kN <= (int)kColO && kColO + kHalfV <= kTmemCols, "TMEM columns");
+static_assert(kSB * kSIssuers * kN <= (int)kColO && kColO + kHalfV <= kTmemCols, "TMEM columns");
 constexpr float kRescaleThreshold = 8.0f;          // log2 units
 constexpr int kBuckets = 1024;
 static_assert(kBuckets == 1024, "the plan kernel scans one bucket per thread of its 1024");
@@ -261,18 +272,18 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->q_empty, kSIssuers);
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&bars->c_full[i], 1);
       mbar_init(&bars->c_empty[i], 1);
     }
     for (int i = 0; i < kSB; ++i) {
-      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_full[i], kSIssuers);
       mbar_init(&bars->p_full[i], 4);
       mbar_init(&bars->pv_done[i], 1);
     }
     mbar_init(&bars->o_free, 4);
-    mbar_init(&bars->drain, 2);  // one commit from each MMA-issuing warp
+    mbar_init(&bars->drain, kSIssuers + 1);  // one commit from each MMA-issuing warp
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -336,8 +347,8 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------- S = Q C^T
+  } else if (s_issuer(warp) >= 0) {
+    // --------------------------------- partial S = Q C^T over three chunks
     constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kN, 0);
     const uint32_t sQa = smem_u32(sQ), sCa = smem_u32(sC);
     uint32_t item_ctr = 0, tile_ctr = 0;
@@ -359,11 +370,11 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
         tc_fence_after();
         if (lane == 0) {
           const uint64_t dc = sw128_desc(sCa + slot * kCBytes, 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < kW / 16; ++kk) {
+          const int part = s_issuer(warp), k0 = part * kMmaPerIssuer;
+          for (int kk = k0; kk < k0 + kMmaPerIssuer; ++kk) {
             const uint32_t oq = (kk / 4) * kQChunk + (kk % 4) * 32;
             const uint32_t oc = (kk / 4) * kCChunk + (kk % 4) * 32;
-            tc_mma_f16(tmem + col_s(sb), desc_advance(dq, oq), desc_advance(dc, oc), idesc_s, kk > 0);
+            tc_mma_f16(tmem + col_s(sb, part), desc_advance(dq, oq), desc_advance(dc, oc), idesc_s, kk > k0);
           }
           tc_commit(&bars->s_full[sb]);
           if (j == I.ntiles - 1) tc_commit(&bars->q_empty);
@@ -456,9 +467,14 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
         tc_fence_after();
         const int ncol = min(kN, I.len - j * kN);
         const uint32_t s_addr = t_lane + col_s(sb);
-        uint32_t v[kN];
+        uint32_t v[kN], v1[kN], v2[kN];
         tmem_ld32(s_addr, v);
+        tmem_ld32(t_lane + col_s(sb, 1), v1);
+        tmem_ld32(t_lane + col_s(sb, 2), v2);
         tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < kN; ++e)
+          v[e] = __float_as_uint((__uint_as_float(v[e]) + __uint_as_float(v1[e])) + __uint_as_float(v2[e]));
         if (ncol < kN) {
 #pragma unroll
           for (int e = 0; e < kN; ++e) v[e] = e < ncol ? v[e] : 0xff800000u;  // -inf: weight 0
