@@ -5,7 +5,7 @@ import torch
 
 import workloads as wl
 
-TOL = {wl.F32: 1e-4, wl.BF16: 1e-2}   # max abs error of o (spec tolerances)
+TOL = {wl.F32: 1e-4, wl.BF16: 1e-2}   # max abs error of o stated for this path
 LSE_TOL = 1e-3
 
 

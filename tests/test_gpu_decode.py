@@ -1,6 +1,6 @@
 """GPU parity of pd_attn_decode against the fp64 oracle (same seeded inputs).
 
-Tolerances from the benchmark spec: max |o - oracle| <= 1e-4 for fp32
+Tolerances stated for this path: max |o - oracle| <= 1e-4 for fp32
 inputs, <= 1e-2 for bf16 inputs (fp32 accumulation), |lse - oracle| <= 1e-3.
 Unused pool pages and tail slots hold NaN, so a stray read shows up."""
 import numpy as np

@@ -1,7 +1,7 @@
 """GPU parity of pd_attn_prefill (tcgen05 tensor-core path) against the fp64
 oracle on the same seeded bf16 inputs.
 
-Tolerance (benchmark spec): max |o - oracle| <= 1e-2 with fp32
+Tolerance stated for this path: max |o - oracle| <= 1e-2 with fp32
 accumulation, |lse - oracle| <= 1e-3. With a bf16 output the stored value is
 additionally rounded to bf16, which alone moves it by up to half a bf16 ulp of
 |o|; the bf16-output checks allow that rounding on top of 1e-2."""
