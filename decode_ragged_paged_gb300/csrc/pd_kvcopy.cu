@@ -134,8 +134,8 @@ __device__ __forceinline__ Unit unit_of(int64_t u, int kp, int hkv, int layers, 
 // Each CTA takes blocks of up to kAppendRows consecutive new-token rows. One
 // thread per row finds the row's request (binary search over the new-token
 // indptr), checks it and looks up its page, all rows at once; then the CTA
-// copies the block's K and V rows (every head) with several 16-byte vectors in
-// flight per thread.
+// copies the block's K and V rows (every head), row by row, with several
+// 16-byte vectors in flight per thread.
 constexpr int kAppendRows = 32;
 
 __global__ void __launch_bounds__(kCopyThreads) kv_append_kernel(const KvCopyParams p, int rows_per_cta) {
@@ -143,6 +143,12 @@ __global__ void __launch_bounds__(kCopyThreads) kv_append_kernel(const KvCopyPar
   const int vpr = p.head_dim * p.elem_size / 16;  // vectors per (token, head) row
   const int hv = p.hkv * vpr;                     // vectors of one token's K (or V)
   const int per_row = 2 * hv;                     // vectors of K and V of one token
+  // pool vector offset of (page, head h, slot) = page * page_vecs + slot * slot_stride + h * head_stride
+  const int64_t page_vecs = (int64_t)p.hkv * p.page_size * vpr;
+  const int64_t slot_stride = slot_stride_vec(p, vpr);
+  const int head_stride = p.nhd ? vpr : p.page_size * vpr;
+  const bool pow2 = (vpr & (vpr - 1)) == 0;
+  const int lg = __ffs(vpr) - 1;
   for (int r0 = blockIdx.x * rows_per_cta; r0 < p.max_new; r0 += gridDim.x * rows_per_cta) {
     const int nrows = min(rows_per_cta, p.max_new - r0);
     if (threadIdx.x < nrows) {
@@ -177,29 +183,33 @@ __global__ void __launch_bounds__(kCopyThreads) kv_append_kernel(const KvCopyPar
       s_slot[threadIdx.x] = slot;
     }
     __syncthreads();
-    const int nvec = nrows * per_row;
-    for (int base = 0; base < nvec; base += kCopyThreads * kUnroll) {
-      uint4 tmp[kUnroll];
-      // Every thread loads its vectors first, then stores them.
+    // Row by row: the row's (page, slot) base once, then its K and V vectors,
+    // several in flight per thread; the head of a vector by a shift when
+    // head_dim * elem_size / 16 is a power of two.
+    for (int k = 0; k < nrows; ++k) {
+      const int page = s_page[k];
+      if (page < 0) continue;
+      const int64_t base = (int64_t)page * page_vecs + (int64_t)s_slot[k] * slot_stride;
+      const int64_t row = (int64_t)(r0 + k) * hv;
+      for (int q0 = 0; q0 < per_row; q0 += kCopyThreads * kUnroll) {
+        uint4 t[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int i = base + u * kCopyThreads + threadIdx.x;
-        if (i < nvec) {
-          const int k = i / per_row, rem = i - k * per_row;
-          const int kv = rem >= hv, w = rem - kv * hv;
-          if (s_page[k] >= 0)
-            tmp[u] = ld_stream(static_cast<const uint4*>(kv ? p.src2 : p.src) + (int64_t)(r0 + k) * hv + w);
+        for (int u = 0; u < kUnroll; ++u) {
+          const int q = q0 + u * kCopyThreads + threadIdx.x;
+          if (q < per_row) {
+            const bool second = q >= hv;
+            t[u] = ld_stream(static_cast<const uint4*>(second ? p.src2 : p.src) + row + (q - (second ? hv : 0)));
+          }
         }
-      }
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int i = base + u * kCopyThreads + threadIdx.x;
-        if (i < nvec) {
-          const int k = i / per_row, rem = i - k * per_row;
-          const int kv = rem >= hv, w = rem - kv * hv;
-          const int h = w / vpr, v = w - h * vpr;
-          if (s_page[k] >= 0)
-            static_cast<uint4*>(kv ? p.dst2 : p.dst)[pool_vec(p, s_page[k], h, s_slot[k], vpr) + v] = tmp[u];
+        for (int u = 0; u < kUnroll; ++u) {
+          const int q = q0 + u * kCopyThreads + threadIdx.x;
+          if (q < per_row) {
+            const bool second = q >= hv;
+            const int w = q - (second ? hv : 0);
+            const int h = pow2 ? w >> lg : w / vpr, v = w - h * vpr;
+            static_cast<uint4*>(second ? p.dst2 : p.dst)[base + (int64_t)h * head_stride + v] = t[u];
+          }
         }
       }
     }
