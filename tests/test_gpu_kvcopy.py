@@ -30,6 +30,9 @@ def _host_bits(a: np.ndarray) -> np.ndarray:
     dict(seed=201, qo=[5, 1, 16, 33], kv=[9, 30, 16, 40], hkv=4, d=128, p=16, dt=wl.BF16),
     dict(seed=202, qo=[3, 7], kv=[3, 11], hkv=2, d=64, p=1, dt=wl.F32),
     dict(seed=203, qo=[20, 1, 1], kv=[70, 64, 65], hkv=3, d=64, p=64, dt=wl.BF16),
+    # head rows of 12 and 5 sixteen-byte vectors: the copy's head index by division
+    dict(seed=207, qo=[7, 19, 1], kv=[40, 19, 33], hkv=3, d=96, p=16, dt=wl.BF16),
+    dict(seed=208, qo=[33, 2], kv=[50, 9], hkv=5, d=40, p=8, dt=wl.BF16),
 ])
 def test_append_small(args):
     case = wl.make_attn_case(args["seed"], args["qo"], args["kv"], args["hkv"], args["hkv"], args["d"], args["p"],
@@ -89,6 +92,22 @@ def test_pack_unpack_small_against_oracle():
                          hc.dst_offsets, total)
     np.testing.assert_array_equal(buf.cpu().numpy(), ref)
     shape = (3, hc.dst_table.num_pages, 4, 64, 64)
+    k_ref, v_ref = wl._poison(shape, hc.dtype), wl._poison(shape, hc.dtype)
+    oracle.kv_unpack(hc.kv_len, hc.dst_table.page_indptr, hc.dst_table.page_indices, ref, hc.dst_offsets,
+                     k_ref, v_ref)
+    np.testing.assert_array_equal(_bits(k_dst), _host_bits(k_ref))
+    np.testing.assert_array_equal(_bits(v_dst), _host_bits(v_ref))
+
+
+def test_pack_unpack_head_dim_not_a_power_of_two():
+    # head rows of 12 sixteen-byte vectors (head_dim 96, bf16)
+    hc = wl.kv_handoff(seed=209, batch=2, layers=2, heads=3, head_dim=96, src_page=16, dst_page=64,
+                       dtype=wl.BF16, kv_lens=[70, 33], src_slack=3, dst_slack=1)
+    buf, k_dst, v_dst = _handoff_roundtrip(hc)
+    ref = oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, hc.k_src, hc.v_src,
+                         hc.dst_offsets, buf.numel())
+    np.testing.assert_array_equal(buf.cpu().numpy(), ref)
+    shape = (2, hc.dst_table.num_pages, 3, 64, 96)
     k_ref, v_ref = wl._poison(shape, hc.dtype), wl._poison(shape, hc.dtype)
     oracle.kv_unpack(hc.kv_len, hc.dst_table.page_indptr, hc.dst_table.page_indices, ref, hc.dst_offsets,
                      k_ref, v_ref)

@@ -127,6 +127,7 @@ def test_mixed_batch_on_nhd_pools():
     dict(seed=405, qo=[5, 1, 16, 33], kv=[9, 30, 16, 40], hkv=4, d=128, p=16, dt=wl.BF16),
     dict(seed=406, qo=[3, 7], kv=[3, 11], hkv=2, d=64, p=1, dt=wl.F32),
     dict(seed=407, qo=[20, 1, 1], kv=[70, 64, 65], hkv=3, d=64, p=64, dt=wl.BF16),
+    dict(seed=409, qo=[7, 19, 1], kv=[40, 19, 33], hkv=3, d=96, p=16, dt=wl.BF16),
 ])
 def test_append_into_nhd_pools(args):
     case = wl.to_nhd(wl.make_attn_case(args["seed"], args["qo"], args["kv"], args["hkv"], args["hkv"], args["d"],
@@ -141,11 +142,13 @@ def test_append_into_nhd_pools(args):
     np.testing.assert_array_equal(_bits(dc.v_pool), _host_bits(v))
 
 
-@pytest.mark.parametrize("src_layout,dst_layout", [("NHD", "NHD"), ("HND", "NHD"), ("NHD", "HND")])
-def test_handoff_between_layouts(src_layout, dst_layout):
+@pytest.mark.parametrize("src_layout,dst_layout,head_dim", [("NHD", "NHD", 64), ("HND", "NHD", 64), ("NHD", "HND", 64),
+                                                          ("NHD", "NHD", 96)])
+def test_handoff_between_layouts(src_layout, dst_layout, head_dim):
     # pack from one layout, unpack into a page-64 pool of the other: the packed
-    # block format does not depend on either pool's layout
-    hc = wl.kv_handoff(seed=408, batch=3, layers=3, heads=4, head_dim=64, src_page=16, dst_page=64,
+    # block format does not depend on either pool's layout (head_dim 96: rows
+    # of 12 sixteen-byte vectors, NHD rows found by division)
+    hc = wl.kv_handoff(seed=408, batch=3, layers=3, heads=4, head_dim=head_dim, src_page=16, dst_page=64,
                        dtype=wl.BF16, kv_lens=[100, 17, 64], src_slack=5, dst_slack=2)
     src = wl.to_nhd(hc) if src_layout == "NHD" else hc
     L, H, D = hc.num_layers, hc.num_kv_heads, hc.head_dim
