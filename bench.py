@@ -491,6 +491,24 @@ def measure_rows(args, dev, peaks) -> dict:
                            "bound": "hbm (128 flop/B < ridge)", "flops": flops, "bytes": pf_bytes}
     except pd.PdError as e:
         rows["prefill"] = {"status": str(e)}
+    # the same path as a prefiller runs it: append, then attention at once
+    # (L2 flushed before the append only, so the appended pages may still be
+    # in L2); the events bracket the attention kernel
+    try:
+        def append_then_prefill():
+            pd.pd_kv_append(w["k_new"], w["v_new"], w["k_pool"], w["v_pool"], w["qo_indptr"], w["kv_len"],
+                            w["page_indptr"], w["page_indices"], max_kv_len=512)
+            pd.pd_attn_prefill(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"], w["page_indices"],
+                               w["qo_indptr"], max_qo_len=512, max_kv_len=512, o=o)
+        ms, kms, hus = timed(append_then_prefill, reps, warm, flush)
+        t = flops / (kms * 1e-3) / 1e12
+        rows["append_then_prefill"] = {"workload": "8 x 512 causal, 40 heads: pd_kv_append then pd_attn_prefill, "
+                                                   "L2 flushed before the append only",
+                                       "ms": round(ms, 5), "prefill_kernel_ms": round(kms, 5),
+                                       "TFLOPs": round(t, 1), "frac_bf16": round(t / peaks["bf16"], 4),
+                                       "call_pair_TFLOPs": round(flops / (ms * 1e-3) / 1e12, 1), "flops": flops}
+    except pd.PdError as e:
+        rows["append_then_prefill"] = {"status": str(e)}
     del w
 
     # a compute-bound causal prefill (same kernel): long sequences put the
