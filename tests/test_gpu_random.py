@@ -1,0 +1,95 @@
+"""Seeded random batches for every attention entry point, against the fp64
+oracle on the same inputs.
+
+Each case draws its shape from its own seed: batch size, query and KV lengths
+(empty requests, single keys, lengths just past a page or a 128-key tile),
+grouped-query head counts, page size, pool layout and output dtype. Calls with
+many query rows per request and decode-like calls run different shapes of the
+tensor-core kernel, and small batches run short persistent grids; all of them
+must meet the same bars as the fixed cases: |o - oracle| <= 1e-2 for bf16
+inputs (fp32 outputs; a bf16 output also carries its own rounding of half a
+bf16 ulp), 1e-4 for fp32 inputs, |lse - oracle| <= 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import decode_ragged_paged_gb300 as pd
+    from gpu_util import DevCase, host_f64, LSE_TOL
+
+
+def _length(rng, lo, hi):
+    """A length in [lo, hi], often at a page or tile edge."""
+    edges = [v for v in (lo, lo + 1, 15, 16, 17, 63, 64, 65, 127, 128, 129, 255, 256, 257, hi) if lo <= v <= hi]
+    return int(rng.choice(edges)) if rng.random() < 0.4 else int(rng.integers(lo, hi + 1))
+
+
+def _case(seed, kind):
+    rng = np.random.default_rng(seed)
+    hkv = int(rng.choice([1, 2, 4]))
+    g = int(rng.choice([1, 2, 3, 4, 8]))
+    page = int(rng.choice([8, 16, 32, 64, 128]))
+    b = int(rng.integers(1, 7))
+    dtype = wl.BF16
+    d = 128
+    if kind == "decode":
+        d = int(rng.choice([64, 128]))
+        if rng.random() < 0.3:
+            dtype = wl.F32
+        qo = [1] * b
+        kv = [_length(rng, 0 if rng.random() < 0.1 else 1, 2500) for _ in range(b)]
+    elif kind == "prefill":
+        qo = [_length(rng, 1, 300) for _ in range(b)]
+        kv = [q + _length(rng, 0, 400) for q in qo]
+    else:  # mixed: some prefill rows, some decodes, some multi-token verifications
+        qo, kv = [], []
+        for _ in range(b):
+            r = rng.random()
+            q = 1 if r < 0.5 else (int(rng.integers(2, 6)) if r < 0.7 else _length(rng, 1, 300))
+            qo.append(q)
+            kv.append(q + _length(rng, 0, 600))
+    # decode rows see every cached key (the bottom-right mask is a no-op for one
+    # row); the oracle takes them unmasked, so that an empty request is valid
+    case = wl.make_attn_case(seed, qo, kv, hkv * g, hkv, d, page, dtype, causal=kind != "decode")
+    if rng.random() < 0.3:
+        case = wl.to_nhd(case)
+    o_dtype = torch.float32 if (dtype == wl.F32 or rng.random() < 0.5) else torch.bfloat16
+    return case, o_dtype
+
+
+def _half_ulp_bf16(x):
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
+    return 2.0 ** (e - 8)
+
+
+@pytest.mark.parametrize("kind", ["decode", "prefill", "mixed"])
+@pytest.mark.parametrize("seed", list(range(700, 708)))
+def test_random_batches(kind, seed):
+    case, o_dtype = _case(seed + {"decode": 0, "prefill": 100, "mixed": 200}[kind], kind)
+    d = DevCase(case)
+    layout = getattr(case, "layout", "HND")
+    if kind == "decode":
+        o, lse = pd.pd_attn_decode(d.q, d.k_pool, d.v_pool, d.kv_len, d.page_indptr, d.page_indices,
+                                   max_kv_len=d.max_kv_len, o_dtype=o_dtype, layout=layout)
+    else:
+        fn = pd.pd_attn_prefill if kind == "prefill" else pd.pd_attn_mixed
+        o, lse = fn(d.q, d.k_pool, d.v_pool, d.kv_len, d.page_indptr, d.page_indices, d.qo_indptr,
+                    max_qo_len=d.max_qo_len, max_kv_len=d.max_kv_len, o_dtype=o_dtype, layout=layout)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attention_case(case)
+    got = host_f64(o)
+    assert np.isfinite(got).all(), "non-finite output"
+    tol = 1e-4 if case.dtype == wl.F32 else 1e-2
+    bound = tol + (_half_ulp_bf16(o_ref) if o_dtype == torch.bfloat16 else 0.0)
+    err = np.abs(got - o_ref)
+    assert np.all(err <= bound), f"{kind} seed {seed}: max |o - oracle| = {err.max()}"
+    lg = lse.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lg), fin)
+    if fin.any():
+        assert float(np.abs(lg[fin] - lse_ref[fin]).max()) <= LSE_TOL
