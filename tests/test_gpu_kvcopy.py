@@ -60,6 +60,57 @@ def test_append_causal_prefill_workload_full():
     np.testing.assert_array_equal(_bits(d.v_pool), _host_bits(v))
 
 
+def _append_with(case, page_indices):
+    """The GPU append of a case with the given page table; returns (pools, status)."""
+    d = DevCase(case)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pd.pd_kv_append(d.k_new, d.v_new, d.k_pool, d.v_pool, d.qo_indptr, d.kv_len, d.page_indptr,
+                    dev_tensor(page_indices.astype(np.int32)), max_kv_len=d.max_kv_len, dev_status=status)
+    torch.cuda.synchronize()
+    return d.k_pool, d.v_pool, int(status.item())
+
+
+def _oracle_append(case):
+    k, v = case.k_pool.copy(), case.v_pool.copy()
+    oracle.kv_append(case.qo_indptr, case.kv_len, case.table.page_indptr, case.table.page_indices,
+                     case.k_new, case.v_new, k, v)
+    return k, v
+
+
+def test_append_reports_a_bad_page_id_and_writes_the_rest():
+    case = wl.make_attn_case(210, [9, 20, 5], [30, 20, 40], 2, 2, 64, 16, wl.BF16, with_new_tokens=True,
+                             num_pages=40)
+    bad_at = int(case.table.page_indptr[1]) + 1  # request 1's second page
+    bad_page = int(case.table.page_indices[bad_at])
+    idx = case.table.page_indices.copy()
+    idx[bad_at] = 1000  # past the 40-page pool
+    k_dev, v_dev, status = _append_with(case, idx)
+    assert status == 3  # bad page table
+    k, v = _oracle_append(case)
+    # every slot matches the oracle's append except those of the page it could not reach
+    k[bad_page], v[bad_page] = case.k_pool[bad_page], case.v_pool[bad_page]
+    np.testing.assert_array_equal(_bits(k_dev), _host_bits(k))
+    np.testing.assert_array_equal(_bits(v_dev), _host_bits(v))
+
+
+def test_append_reports_bad_lengths_and_writes_the_rest():
+    case = wl.make_attn_case(211, [9, 20, 5], [30, 20, 40], 2, 2, 64, 16, wl.BF16, with_new_tokens=True,
+                             num_pages=40)
+    d = DevCase(case)
+    kv = case.kv_len.astype(np.int32).copy()
+    kv[1] = 12  # request 1 brings 20 new tokens but claims 12 cached
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pd.pd_kv_append(d.k_new, d.v_new, d.k_pool, d.v_pool, d.qo_indptr, dev_tensor(kv), d.page_indptr,
+                    d.page_indices, max_kv_len=d.max_kv_len, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 2  # bad length
+    k, v = _oracle_append(case)
+    for pg in case.table.page_indices[case.table.page_indptr[1]:case.table.page_indptr[2]]:
+        k[pg], v[pg] = case.k_pool[pg], case.v_pool[pg]  # request 1 left unwritten
+    np.testing.assert_array_equal(_bits(d.k_pool), _host_bits(k))
+    np.testing.assert_array_equal(_bits(d.v_pool), _host_bits(v))
+
+
 def _handoff_roundtrip(hc: wl.HandoffCase, check_oracle_layers=None):
     es = wl.element_size(hc.dtype)
     L, H, D = hc.num_layers, hc.num_kv_heads, hc.head_dim
