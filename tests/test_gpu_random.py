@@ -1,4 +1,4 @@
-"""Seeded random batches for every attention entry point, against the fp64
+"""Seeded random batches for every attention entry point (and MLA decode), against the fp64
 oracle on the same inputs.
 
 Each case draws its shape from its own seed: batch size, query and KV lengths
@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     import decode_ragged_paged_gb300 as pd
-    from gpu_util import DevCase, host_f64, LSE_TOL
+    from gpu_util import DevCase, dev_tensor, host_f64, LSE_TOL
 
 
 def _length(rng, lo, hi):
@@ -88,6 +88,33 @@ def test_random_batches(kind, seed):
     bound = tol + (_half_ulp_bf16(o_ref) if o_dtype == torch.bfloat16 else 0.0)
     err = np.abs(got - o_ref)
     assert np.all(err <= bound), f"{kind} seed {seed}: max |o - oracle| = {err.max()}"
+    lg = lse.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lg), fin)
+    if fin.any():
+        assert float(np.abs(lg[fin] - lse_ref[fin]).max()) <= LSE_TOL
+
+
+@pytest.mark.parametrize("seed", list(range(1000, 1004)))
+def test_random_mla_batches(seed):
+    # MLA decode: head count, page size and lengths drawn per seed (empty
+    # requests and single keys included); a long request is split into chunks
+    rng = np.random.default_rng(seed)
+    hq = int(rng.choice([1, 8, 16, 64, 128]))
+    page = int(rng.choice([16, 32, 64, 128, 256]))
+    kv = [_length(rng, 0, 3000) for _ in range(int(rng.integers(1, 9)))]
+    c = wl.mla_case(seed, kv, num_qo_heads=hq, page_size=page)
+    o_dtype = torch.float32 if rng.random() < 0.5 else torch.bfloat16
+    o, lse = pd.pd_mla_decode(dev_tensor(c.q), dev_tensor(c.kv_pool), dev_tensor(c.kv_len.astype(np.int32)),
+                              dev_tensor(c.table.page_indptr), dev_tensor(c.table.page_indices), kv_lora_rank=c.d_c,
+                              sm_scale=c.sm_scale, max_kv_len=int(c.kv_len.max()), o_dtype=o_dtype)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.mla_decode(c.kv_len, c.table.page_indptr, c.table.page_indices, c.q, c.kv_pool, c.d_c,
+                                       c.sm_scale)
+    got = host_f64(o)
+    assert np.isfinite(got).all()
+    bound = 1e-2 + (_half_ulp_bf16(o_ref) if o_dtype == torch.bfloat16 else 0.0)
+    assert np.all(np.abs(got - o_ref) <= bound), f"seed {seed}: max |o - oracle| = {np.abs(got - o_ref).max()}"
     lg = lse.cpu().numpy().astype(np.float64)
     fin = np.isfinite(lse_ref)
     assert np.array_equal(np.isfinite(lg), fin)
