@@ -13,8 +13,14 @@
 // the latent row of each token is read once per request. O for 128 rows x 512
 // values fills all of TMEM, so each (request, chunk) is run by a pair of CTAs,
 // each owning 256 of the value columns (half h: columns [256h, 256h + 256));
-// both compute the full 128 x 32 score tile from the same latent tiles, the
+// both compute the full 128 x 64 score tile from the same latent tiles, the
 // second read of a tile coming from L2.
+//
+// Shared memory holds Q (144 KiB) for the whole request, so a 64-token tile
+// (72 KiB) is not double-buffered whole: it streams through in nine column
+// chunks of 64 tokens x 64 values (8 KiB), and this half's value columns are
+// read a second time (from L2) into a slot of their own for O += P C_h. Each
+// MMA of the score product then reads its 4 KiB slice of Q for 64 keys.
 //
 // Three launches, each a programmatic dependent of the one before:
 //   1. plan    one CTA: validates requests, picks the chunk length from the
@@ -23,15 +29,19 @@
 //   2. decode  persistent CTA pairs (one CTA per SM) walk the list in
 //              serpentine order. Warp roles:
 //                warp 0    TMA producer: the request's Q tile (9 boxes of 64
-//                          columns x 128 heads) and 32-token latent tiles
-//                          (2-slot ring, 9 x 128-byte-swizzled boxes per page);
-//                warps 1, 6, 8  issue S = Q C^T as three partial products
-//                          over three column chunks each (12 MMAs of K 16
-//                          apiece: one thread issues a tcgen05.mma about
-//                          every 94 cycles whatever N, so one issuer would
-//                          bound the tile); warp 1 also allocates TMEM;
+//                          columns x 128 heads) and each tile's nine column
+//                          chunks (128-byte-swizzled boxes, one per page
+//                          run), even chunks to one 3-slot ring, odd chunks
+//                          to another;
+//                warp 8    TMA producer of the value slot (this half's four
+//                          column chunks of the tile);
+//                warps 1, 6  issue S = Q C^T as two partial products, over
+//                          the even and the odd column chunks (one thread
+//                          issues a tcgen05.mma about every 94 cycles
+//                          whatever N, so one issuer would bound the tile);
+//                          warp 1 also allocates TMEM;
 //                warp 7    issues O += P C_h with P read from TMEM;
-//                warps 2-5 one head per thread: S = the sum of the three
+//                warps 2-5 one head per thread: S = the sum of the two
 //                          partials, online softmax (lazy O
 //                          rescale), the epilogue (final o and lse, or a fp32
 //                          partial for a request split into chunks);
@@ -53,24 +63,35 @@ constexpr int kDr = 64;                  // rope width (scores only)
 constexpr int kW = kDc + kDr;            // stored row: 576 values
 constexpr int kWC = kW / 64;             // 9 column chunks of 64 values (128 bytes)
 constexpr int kRows = 128;               // tile rows: query heads, zero-padded
-constexpr int kN = 32;                   // tokens per latent tile
+constexpr int kN = 64;                   // tokens per latent tile
 constexpr int kHalfV = kDc / 2;          // value columns per CTA of a pair
 constexpr int kVChunks = kHalfV / 64;    // 4 column chunks per half
 constexpr int kThreadsMla = 288;         // 9 warps
 constexpr int kWarpPV = 7;
-constexpr int kSIssuers = 3;             // warps issuing the partial score products
-constexpr int kMmaPerIssuer = (kW / 16) / kSIssuers;
-static_assert(kMmaPerIssuer * kSIssuers * 16 == kW && kMmaPerIssuer % 4 == 0, "issuers take whole chunks");
-// index of the partial product warp w issues, or -1
-__device__ __forceinline__ int s_issuer(int w) { return w == 1 ? 0 : w == 6 ? 1 : w == 8 ? 2 : -1; }
-constexpr int kSlots = 2;                // latent tile ring
+constexpr int kWarpV = 8;                // producer of the value slot
+#ifndef PD_MLA_ISSUERS
+#define PD_MLA_ISSUERS 2
+#endif
+constexpr int kSIssuers = PD_MLA_ISSUERS;  // warps issuing the partial score products
+static_assert(kSIssuers == 1 || kSIssuers == 2, "one or two score issuers");
+// index of the partial product warp w issues, or -1; partial i takes the
+// column chunks c with c % kSIssuers == i
+__device__ __forceinline__ int s_issuer(int w) { return w == 1 ? 0 : (w == 6 && kSIssuers > 1) ? 1 : -1; }
+constexpr int kRing = 6 / kSIssuers;     // column-chunk ring of each issuer
+// tile t's column chunk c travels through ring c % kSIssuers as that ring's
+// entry ring_seq(t, c) (with two rings: five chunks per tile in ring 0, four in ring 1)
+__device__ __forceinline__ uint32_t ring_seq(uint32_t t, int c) {
+  const int r = c % kSIssuers;
+  return t * (uint32_t)((kWC - r + kSIssuers - 1) / kSIssuers) + (uint32_t)(c / kSIssuers);
+}
 constexpr int kSB = 2;                   // S / P buffers in TMEM
 constexpr uint32_t kQChunk = kRows * 128;          // 16 KiB: 128 rows x 64 values
 constexpr uint32_t kQBytes = kWC * kQChunk;        // 144 KiB
-constexpr uint32_t kCChunk = kN * 128;             // 4 KiB: 32 tokens x 64 values
-constexpr uint32_t kCBytes = kWC * kCChunk;        // 36 KiB
+constexpr uint32_t kCChunk = kN * 128;             // 8 KiB: 64 tokens x 64 values
+constexpr uint32_t kVBytes = kVChunks * kCChunk;   // 32 KiB: this half's value columns of a tile
 constexpr uint32_t kOffC = kQBytes;
-constexpr uint32_t kOffBar = kQBytes + kSlots * kCBytes;
+constexpr uint32_t kOffV = kOffC + kSIssuers * kRing * kCChunk;
+constexpr uint32_t kOffBar = kOffV + kVBytes;
 constexpr size_t kMlaSmem = kOffBar + 256 + 1024;
 static_assert(kMlaSmem <= 227 * 1024, "shared memory");
 constexpr uint32_t kTmemCols = 512;
@@ -78,27 +99,18 @@ constexpr uint32_t kTmemCols = 512;
 __device__ __forceinline__ uint32_t col_s(int b, int part = 0) { return (uint32_t)(b * kSIssuers + part) * kN; }
 constexpr uint32_t kColO = 256;                    // O half: columns [256, 512)
 static_assert(kSB * kSIssuers * kN <= (int)kColO && kColO + kHalfV <= kTmemCols, "TMEM columns");
+static_assert(kCChunk % 1024 == 0 && kOffV % 1024 == 0, "128-byte-swizzled chunks start on 1 KiB");
 constexpr float kRescaleThreshold = 8.0f;          // log2 units
 constexpr int kBuckets = 1024;
 static_assert(kBuckets == 1024, "the plan kernel scans one bucket per thread of its 1024");
 
 struct Bars {
-  uint64_t q_full, q_empty, c_full[kSlots], c_empty[kSlots];
+  uint64_t q_full, q_empty, c_full[kSIssuers][kRing], c_empty[kSIssuers][kRing], v_full, v_empty;
   uint64_t s_full[kSB], p_full[kSB], pv_done[kSB], o_free, drain;
   uint32_t tmem_slot;
   int abort;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
-
-// P: 32 bf16 weights of this thread's row as 16 columns of bf16 pairs.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
 
 // A (request, chunk) pair of the work list and what the kernels need of it.
 struct MItem {
@@ -265,6 +277,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sC = smem + kOffC;
+  uint8_t* sV = smem + kOffV;
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -273,10 +286,13 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, kSIssuers);
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&bars->c_full[i], 1);
-      mbar_init(&bars->c_empty[i], 1);
-    }
+    for (int r = 0; r < kSIssuers; ++r)
+      for (int i = 0; i < kRing; ++i) {
+        mbar_init(&bars->c_full[r][i], 1);
+        mbar_init(&bars->c_empty[r][i], 1);
+      }
+    mbar_init(&bars->v_full, 1);
+    mbar_init(&bars->v_empty, 1);
     for (int i = 0; i < kSB; ++i) {
       mbar_init(&bars->s_full[i], kSIssuers);
       mbar_init(&bars->p_full[i], 4);
@@ -302,55 +318,77 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
   pdl_wait_primary();  // the plan kernel's list and chunk length
   pdl_launch_dependents();
   const int n_items = (blockIdx.x < 2 * pairs) ? p.hdr[0] : 0;  // an odd last CTA has no partner
+  const int pb = p.page_size < kN ? p.page_size : kN;  // tokens per box
+  const int nb = kN / pb;                              // boxes per column chunk
 
-  if (warp == 0) {
-    // ------------------------------------------------------------- producer
-    const int pb = p.page_size < kN ? p.page_size : kN;  // tokens per box
-    const int nb = kN / pb;                              // boxes per column chunk
+  if (warp == 0 || warp == kWarpV) {
+    // ----------------------------------------------------------- producers
+    // warp 0: the request's Q tile, then every tile's nine column chunks of
+    // 64 tokens x 64 values, in order, through the two issuers' rings (one
+    // consumer per ring); warp 8: this half's four value
+    // chunks of every tile into the value slot, once the previous tile's
+    // O += P C_h has read it (the second read of those rows comes from L2)
+    const bool is_v = warp == kWarpV;
     uint32_t item_ctr = 0, tile_ctr = 0;
     bool ok = true;
     for (int k = 0; ok; ++k, ++item_ctr) {
       const int idx = pair_item(k, pair, pairs);
       if (idx >= n_items) break;
       const MItem I = mla_item(p, idx);
-      // the previous item's S products have all completed before Q is replaced
-      ok = warp_mbar_wait(&bars->q_empty, (item_ctr & 1u) ^ 1u, abort, p.status);
-      if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&bars->q_full, kQBytes);
-      __syncwarp();
-      if (lane < kWC) tma_load_3d(sQ + lane * kQChunk, &tm_q, lane * 64, 0, I.r, &bars->q_full);
+      if (!is_v) {
+        // the previous item's S products have all completed before Q is replaced
+        ok = warp_mbar_wait(&bars->q_empty, (item_ctr & 1u) ^ 1u, abort, p.status);
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(&bars->q_full, kQBytes);
+        __syncwarp();
+        if (lane < kWC) tma_load_3d(sQ + lane * kQChunk, &tm_q, lane * 64, 0, I.r, &bars->q_full);
+      }
       for (int j = 0; j < I.ntiles && ok; ++j, ++tile_ctr) {
-        const int slot = tile_ctr % kSlots;
-        // page of this lane's box, read before the slot wait
+        // page of box `sub` (lanes below nb), read before any slot wait
         int pid = p.num_pages, soff = 0;
-        const int box = lane;
-        if (box < kWC * nb) {
-          const int tok = I.t0 + j * kN + (box % nb) * pb;
+        const int sub = lane % nb;
+        {
+          const int tok = I.t0 + j * kN + sub * pb;
           const int pidx = tok / p.page_size;
           soff = tok % p.page_size;
           if (pidx < I.need) {
             pid = __ldg(p.page_indices + I.pbase + pidx);
             if (pid < 0 || pid >= p.num_pages) {
-              report(p.status, PD_DEV_BAD_PAGE_TABLE);
+              if (lane < nb) report(p.status, PD_DEV_BAD_PAGE_TABLE);
               pid = p.num_pages;  // out of range: the box arrives as zeros
             }
           }
         }
-        ok = warp_mbar_wait(&bars->c_empty[slot], ((tile_ctr / kSlots) & 1u) ^ 1u, abort, p.status);
-        if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(&bars->c_full[slot], kCBytes);
-        __syncwarp();
-        if (box < kWC * nb) {
-          const int chunk = box / nb, sub = box % nb;
-          tma_load_4d(sC + slot * kCBytes + chunk * kCChunk + sub * pb * 128, &tm_c, chunk * 64, soff, 0, pid,
-                      &bars->c_full[slot]);
+        if (is_v) {
+          ok = warp_mbar_wait(&bars->v_empty, (tile_ctr & 1u) ^ 1u, abort, p.status);
+          if (!ok) break;
+          if (lane == 0) mbar_arrive_expect_tx(&bars->v_full, kVBytes);
+          __syncwarp();
+          if (lane < kVChunks * nb) {
+            const int ch = lane / nb;
+            tma_load_4d(sV + ch * kCChunk + sub * pb * 128, &tm_c, (half * kVChunks + ch) * 64, soff, 0, pid,
+                        &bars->v_full);
+          }
+        } else {
+          for (int c = 0; c < kWC && ok; ++c) {
+            const int r = c % kSIssuers;
+            const uint32_t seq = ring_seq(tile_ctr, c), slot = seq % kRing;
+            ok = warp_mbar_wait(&bars->c_empty[r][slot], ((seq / kRing) & 1u) ^ 1u, abort, p.status);
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(&bars->c_full[r][slot], kCChunk);
+            __syncwarp();
+            if (lane < nb)
+              tma_load_4d(sC + (r * kRing + slot) * kCChunk + sub * pb * 128, &tm_c, c * 64, soff, 0, pid,
+                          &bars->c_full[r][slot]);
+          }
         }
       }
     }
   } else if (s_issuer(warp) >= 0) {
-    // --------------------------------- partial S = Q C^T over three chunks
+    // ------------------ partial S = Q C^T over this warp's column chunks
     constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kN, 0);
     const uint32_t sQa = smem_u32(sQ), sCa = smem_u32(sC);
+    const int part = s_issuer(warp);
     uint32_t item_ctr = 0, tile_ctr = 0;
     bool ok = true;
     for (int k = 0; ok; ++k, ++item_ctr) {
@@ -361,21 +399,30 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
       if (!ok) break;
       tc_fence_after();
       const uint64_t dq = sw128_desc(sQa, 16, 1024);
-      for (int j = 0; j < I.ntiles; ++j, ++tile_ctr) {
-        const int slot = tile_ctr % kSlots, sb = tile_ctr % kSB;
-        ok = warp_mbar_wait(&bars->c_full[slot], (tile_ctr / kSlots) & 1u, abort, p.status) &&
-             (tile_ctr < (uint32_t)kSB ||
-              warp_mbar_wait(&bars->pv_done[sb], ((tile_ctr - kSB) / kSB) & 1u, abort, p.status));
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint64_t dc = sw128_desc(sCa + slot * kCBytes, 16, 1024);
-          const int part = s_issuer(warp), k0 = part * kMmaPerIssuer;
-          for (int kk = k0; kk < k0 + kMmaPerIssuer; ++kk) {
-            const uint32_t oq = (kk / 4) * kQChunk + (kk % 4) * 32;
-            const uint32_t oc = (kk / 4) * kCChunk + (kk % 4) * 32;
-            tc_mma_f16(tmem + col_s(sb, part), desc_advance(dq, oq), desc_advance(dc, oc), idesc_s, kk > k0);
+      for (int j = 0; j < I.ntiles && ok; ++j, ++tile_ctr) {
+        const int sb = tile_ctr % kSB;
+        // S buffer sb is free once the P C product of two tiles back is done
+        if (tile_ctr >= (uint32_t)kSB) {
+          ok = warp_mbar_wait(&bars->pv_done[sb], ((tile_ctr - kSB) / kSB) & 1u, abort, p.status);
+          if (!ok) break;
+        }
+        for (int c = part; c < kWC; c += kSIssuers) {
+          const uint32_t seq = ring_seq(tile_ctr, c), slot = seq % kRing;
+          ok = warp_mbar_wait(&bars->c_full[part][slot], (seq / kRing) & 1u, abort, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint64_t dc = sw128_desc(sCa + (part * kRing + slot) * kCChunk, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_f16(tmem + col_s(sb, part), desc_advance(dq, c * kQChunk + kk * 32), desc_advance(dc, kk * 32),
+                         idesc_s, (c > part || kk > 0) ? 1u : 0u);
+            tc_commit(&bars->c_empty[part][slot]);
           }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) {
           tc_commit(&bars->s_full[sb]);
           if (j == I.ntiles - 1) tc_commit(&bars->q_empty);
         }
@@ -395,7 +442,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
   } else if (warp == kWarpPV) {
     // ---------------------------------------------------------- O += P C_h
     constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, kHalfV, 1);
-    const uint32_t sCa = smem_u32(sC);
+    const uint32_t sVa = smem_u32(sV);
     uint32_t item_ctr = 0, tile_ctr = 0;
     bool ok = true;
     for (int k = 0; ok; ++k, ++item_ctr) {
@@ -408,18 +455,18 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
         if (!ok) break;
       }
       for (int j = 0; j < I.ntiles; ++j, ++tile_ctr) {
-        const int slot = tile_ctr % kSlots, sb = tile_ctr % kSB;
-        ok = warp_mbar_wait(&bars->p_full[sb], (tile_ctr / kSB) & 1u, abort, p.status);
+        const int sb = tile_ctr % kSB;
+        ok = warp_mbar_wait(&bars->p_full[sb], (tile_ctr / kSB) & 1u, abort, p.status) &&
+             warp_mbar_wait(&bars->v_full, tile_ctr & 1u, abort, p.status);
         if (!ok) break;
-        // tokens past the chunk in its last tile: zero this half's value rows so
+        // tokens past the chunk in its last tile: zero their value rows so
         // that stale or poisoned values cannot reach O through a zero weight
         const int valid = I.len - j * kN;
-        const uint32_t ct = sCa + slot * kCBytes + half * kVChunks * kCChunk;
         if (valid < kN) {
           for (int i = lane; i < (kN - valid) * 8 * kVChunks; i += 32) {
             const int ch = i / ((kN - valid) * 8), rem = i % ((kN - valid) * 8);
             const int rr = valid + rem / 8, c16 = rem % 8;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(ct + ch * kCChunk + rr * 128 + c16 * 16),
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(sVa + ch * kCChunk + rr * 128 + c16 * 16),
                          "r"(0)
                          : "memory");
           }
@@ -428,14 +475,14 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
         }
         tc_fence_after();
         if (lane == 0) {
-          const uint64_t dv = sw128_desc(ct, kCChunk, 1024);
+          const uint64_t dv = sw128_desc(sVa, kCChunk, 1024);
           const uint32_t pa = tmem + col_s(sb);
 #pragma unroll
           for (int kk = 0; kk < kN / 16; ++kk)
             tc_mma_f16_tmem_a(tmem + kColO, pa + 8 * kk, desc_advance(dv, kk * 2048), idesc_pv,
                               (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&bars->pv_done[sb]);
-          tc_commit(&bars->c_empty[slot]);
+          tc_commit(&bars->v_empty);
         }
         __syncwarp();
       }
@@ -467,14 +514,21 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
         tc_fence_after();
         const int ncol = min(kN, I.len - j * kN);
         const uint32_t s_addr = t_lane + col_s(sb);
-        uint32_t v[kN], v1[kN], v2[kN];
-        tmem_ld32(s_addr, v);
-        tmem_ld32(t_lane + col_s(sb, 1), v1);
-        tmem_ld32(t_lane + col_s(sb, 2), v2);
-        tmem_wait_ld();
+        // S (with two issuers: the sum of the partial products over the even
+        // and the odd column chunks)
+        uint32_t v[kN];
+        tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        if (kSIssuers > 1) {
+          uint32_t v1[kN];
+          tmem_ld32(t_lane + col_s(sb, 1), *reinterpret_cast<uint32_t(*)[32]>(v1));
+          tmem_ld32(t_lane + col_s(sb, 1) + 32, *reinterpret_cast<uint32_t(*)[32]>(v1 + 32));
+          tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < kN; ++e)
-          v[e] = __float_as_uint((__uint_as_float(v[e]) + __uint_as_float(v1[e])) + __uint_as_float(v2[e]));
+          for (int e = 0; e < kN; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(v1[e]));
+        } else {
+          tmem_wait_ld();
+        }
         if (ncol < kN) {
 #pragma unroll
           for (int e = 0; e < kN; ++e) v[e] = e < ncol ? v[e] : 0xff800000u;  // -inf: weight 0
@@ -528,7 +582,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
           ls2[(e / 2) & 1] = fadd2(ls2[(e / 2) & 1], pe);
         }
         l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
-        tmem_st16(s_addr, w);
+        tmem_st32(s_addr, w);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -650,7 +704,7 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(const MlaParams p) {
 int mla_supported(int32_t d_c, int32_t d_r, int32_t dtype, int32_t hq, int32_t page_size) {
   if (d_c != kDc || d_r != kDr || dtype != PD_BF16) return PD_ERR_UNSUPPORTED;
   if (hq < 1 || hq > kRows) return PD_ERR_UNSUPPORTED;
-  // 32-token tiles of whole boxes, at most 18 boxes for the producer warp's lanes
+  // 64-token tiles of whole boxes: at most four boxes per column chunk, 16 for the value slot
   if (page_size < 16 || page_size > 256 || (page_size & (page_size - 1)) != 0) return PD_ERR_UNSUPPORTED;
   return PD_OK;
 }
