@@ -58,8 +58,8 @@ def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
 
 
 def test_mla_small_all_heads():
-    # lengths around the 32-token tile and one request split into chunks
-    c = wl.mla_case(501, [1, 31, 32, 33, 700], num_qo_heads=128, page_size=64)
+    # lengths around the 32- and 64-token edges, and one request split into chunks
+    c = wl.mla_case(501, [1, 31, 32, 33, 63, 64, 65, 700], num_qo_heads=128, page_size=64)
     o, lse = run_mla(c)
     assert pd.pd_last_kernel() == "mla_decode_kernel"
     check(c, o, lse)
