@@ -19,6 +19,7 @@
 //              and the consumer warps compute the scores, the chunk softmax and
 //              the weighted value sum in fp32;
 //   3. merge   chunks of one request are combined by their log-sum-exp.
+#include <atomic>
 #include <math.h>
 
 #include "pd_common.cuh"
@@ -716,11 +717,14 @@ cudaError_t launch_dependent(Kernel kernel, dim3 grid, dim3 block, size_t smem, 
 template <int ES, int D, int GS>
 int run_decode(DecodeParams& p, cudaStream_t stream) {
   constexpr size_t smem = decode_smem_bytes<ES, D, GS>();
-  static int configured_device = -1;
-  static int blocks_per_sm = 0;
+  // per device: 1 + resident CTAs per SM once the kernel's shared-memory
+  // attribute is set there (0: not yet); callers may run on several threads
+  static std::atomic<int> configured[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;
-  if (configured_device != dev) {
+  const bool cached = dev >= 0 && dev < 64;
+  int blocks_per_sm = cached ? configured[dev].load(std::memory_order_acquire) - 1 : 0;
+  if (blocks_per_sm < 1) {
     if (cudaFuncSetAttribute(decode_kernel<ES, D, GS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return PD_ERR_CUDA;
@@ -728,7 +732,7 @@ int run_decode(DecodeParams& p, cudaStream_t stream) {
                                                       smem) != cudaSuccess)
       return PD_ERR_CUDA;
     if (blocks_per_sm < 1) blocks_per_sm = 1;
-    configured_device = dev;
+    if (cached) configured[dev].store(blocks_per_sm + 1, std::memory_order_release);
   }
   decode_plan_kernel<<<1, 1024, 0, stream>>>(p);
   const int64_t max_items = (int64_t)p.max_chunks * p.items_per_chunk;

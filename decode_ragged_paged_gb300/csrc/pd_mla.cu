@@ -48,6 +48,7 @@
 //   3. merge   requests split into chunks: log-sum-exp merge of the partials.
 // Every wait is bounded; on a timeout the CTA records PD_DEV_TIMEOUT, drains
 // and frees its TMEM.
+#include <atomic>
 #include <math.h>
 
 #include "pd_common.cuh"
@@ -736,14 +737,17 @@ int launch_mla(MlaParams& p, const void* q, const void* kv_pool, cudaStream_t st
   if (!make_rows_map(&tq, q, PD_BF16, p.batch, p.hq, kW, 64, 1, true, kRows) ||
       !make_pool_map(&tc, kv_pool, PD_BF16, p.num_pages, 1, p.page_size, kW, 64, pb, true))
     return PD_ERR_CUDA;
-  static int configured_device = -1;
+  // per device: whether the kernel's shared-memory attribute is set there
+  // (callers may run on several threads)
+  static std::atomic<bool> configured[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;
-  if (configured_device != dev) {
+  const bool cached = dev >= 0 && dev < 64;
+  if (!cached || !configured[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMlaSmem) !=
         cudaSuccess)
       return PD_ERR_CUDA;
-    configured_device = dev;
+    if (cached) configured[dev].store(true, std::memory_order_release);
   }
   last_kernel() = "mla_decode_kernel";
   mla_plan_kernel<<<1, 1024, 0, stream>>>(p);

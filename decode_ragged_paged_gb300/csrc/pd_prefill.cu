@@ -29,6 +29,7 @@
 //             stored by TMA, other tiles stored row by row.
 // Every wait is bounded; on a timeout the CTA records PD_DEV_TIMEOUT, drains
 // and frees its TMEM.
+#include <atomic>
 #include <math.h>
 #include <string.h>
 
@@ -753,13 +754,16 @@ int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const vo
   // deeper K ring and direct O stores.
   const bool long_q = (int64_t)p.total_qo * 2 >= (int64_t)kBM * p.batch;
   auto kernel = long_q ? prefill_kernel<3, 2, true> : prefill_kernel<2, 3, false>;
-  static int configured_device[2] = {-1, -1};
+  // per device and kernel shape: whether the shared-memory attribute is set
+  // there (callers may run on several threads)
+  static std::atomic<bool> configured[64][2];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;
-  if (configured_device[long_q] != dev) {
+  const bool cached = dev >= 0 && dev < 64;
+  if (!cached || !configured[dev][long_q].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrefillSmem) != cudaSuccess)
       return PD_ERR_CUDA;
-    configured_device[long_q] = dev;
+    if (cached) configured[dev][long_q].store(true, std::memory_order_release);
   }
   last_kernel() = "prefill_kernel";
   prefill_plan_kernel<<<1, 1024, 0, stream>>>(p);
