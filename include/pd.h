@@ -81,7 +81,7 @@ extern "C" {
 typedef enum {
   PD_OK = 0,
   PD_ERR_INVALID_ARG = -1, /* null pointer, negative or inconsistent host-side size */
-  PD_ERR_UNSUPPORTED = -2, /* valid request this build does not implement */
+  PD_ERR_UNSUPPORTED = -2, /* valid request the library does not implement */
   PD_ERR_WORKSPACE = -3,   /* workspace smaller than pd_attn_workspace_size() */
   PD_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed */
   PD_ERR_TIMEOUT = -5      /* a host-side wait (the layer messenger) ran out */
