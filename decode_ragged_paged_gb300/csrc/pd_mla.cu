@@ -70,10 +70,9 @@ constexpr int kVChunks = kHalfV / 64;    // 4 column chunks per half
 constexpr int kThreadsMla = 288;         // 9 warps
 constexpr int kWarpPV = 7;
 constexpr int kWarpV = 8;                // producer of the value slot
-#ifndef PD_MLA_ISSUERS
-#define PD_MLA_ISSUERS 2
-#endif
-constexpr int kSIssuers = PD_MLA_ISSUERS;  // warps issuing the partial score products
+// warps issuing the partial score products (one issuer, with one 6-slot ring,
+// was measured slower: a thread issues an MMA about every 94 cycles)
+constexpr int kSIssuers = 2;
 static_assert(kSIssuers == 1 || kSIssuers == 2, "one or two score issuers");
 // index of the partial product warp w issues, or -1; partial i takes the
 // column chunks c with c % kSIssuers == i
