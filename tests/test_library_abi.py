@@ -181,6 +181,7 @@ def _mla_desc(**kw):
     (dict(kv_dtype=pd.PD_F32), pd.PD_ERR_UNSUPPORTED),
     (dict(page_size=8), pd.PD_ERR_UNSUPPORTED),
     (dict(page_size=48), pd.PD_ERR_UNSUPPORTED),
+    (dict(page_size=512), pd.PD_ERR_UNSUPPORTED),        # above the largest supported page
     (dict(o_dtype=9), pd.PD_ERR_INVALID_ARG),
 ])
 def test_mla_rejects_bad_descriptor(lib, kw, code):
