@@ -40,7 +40,8 @@
 //                          issues a tcgen05.mma about every 94 cycles
 //                          whatever N, so one issuer would bound the tile);
 //                          warp 1 also allocates TMEM;
-//                warp 7    issues O += P C_h with P read from TMEM;
+//                warp 7    issues O += P C_h with P read from TMEM (bf16
+//                          pairs and their rounding remainders);
 //                warps 2-5 one head per thread: S = the sum of the two
 //                          partials, online softmax (lazy O
 //                          rescale), the epilogue (final o and lse, or a fp32
@@ -139,6 +140,36 @@ __device__ __forceinline__ MItem mla_item(const MlaParams& p, int idx) {
 
 __device__ __forceinline__ int pair_item(int k, int pair, int pairs) {
   return k * pairs + ((k & 1) ? pairs - 1 - pair : pair);
+}
+
+// P = 2^(s * scale - m) for one head's row of a 64-token tile, written over
+// the first partial-score buffer in TMEM; l accumulates the fp32 weights. Each
+// 32-column chunk of S is replaced by its own words: per 16 keys, 8 words of
+// bf16 pairs, then 8 words of their rounding remainders bf16(p - hi), and
+// P C_h adds both products, so it sees p to about 16 bits. MLA's scores, over
+// 576-value rows, are peaked: a few keys carry most of the weight at any
+// length, and bf16 weights alone (8 significant bits) would move such outputs
+// by several 1e-3.
+__device__ __forceinline__ void mla_write_p(const uint32_t (&v)[kN], uint32_t s_addr, float2 sc2, float2 nm2,
+                                            float& l) {
+  float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int c = 0; c < kN / 32; ++c) {
+    uint32_t w[32];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const int x0 = 32 * c + e;
+      const float2 x = ffma2(make_float2(__uint_as_float(v[x0]), __uint_as_float(v[x0 + 1])), sc2, nm2);
+      const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+      const int wi = (e / 16) * 16 + (e % 16) / 2;  // word of this pair in the chunk
+      w[wi] = pack_bf16x2(pe.x, pe.y);
+      const float2 r = ffma2(make_float2(bf16_lo(w[wi]), bf16_hi(w[wi])), make_float2(-1.f, -1.f), pe);  // exact
+      w[wi + 8] = pack_bf16x2(r.x, r.y);
+      ls2[(e / 2) & 1] = fadd2(ls2[(e / 2) & 1], pe);
+    }
+    tmem_st32(s_addr + 32 * c, w);
+  }
+  l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
 }
 
 }  // namespace
@@ -477,10 +508,14 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
         if (lane == 0) {
           const uint64_t dv = sw128_desc(sVa, kCChunk, 1024);
           const uint32_t pa = tmem + col_s(sb);
+          // keys 16kk .. 16kk + 15: P's bf16 pairs in columns 16kk .. 16kk + 7,
+          // their rounding remainders in 16kk + 8 .. 16kk + 15
 #pragma unroll
-          for (int kk = 0; kk < kN / 16; ++kk)
-            tc_mma_f16_tmem_a(tmem + kColO, pa + 8 * kk, desc_advance(dv, kk * 2048), idesc_pv,
+          for (int kk = 0; kk < kN / 16; ++kk) {
+            tc_mma_f16_tmem_a(tmem + kColO, pa + 16 * kk, desc_advance(dv, kk * 2048), idesc_pv,
                               (j > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_f16_tmem_a(tmem + kColO, pa + 16 * kk + 8, desc_advance(dv, kk * 2048), idesc_pv, 1u);
+          }
           tc_commit(&bars->pv_done[sb]);
           tc_commit(&bars->v_empty);
         }
@@ -572,17 +607,7 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
         }
         m = m_new;
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m, -m);
-        float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        uint32_t w[kN / 2];
-#pragma unroll
-        for (int e = 0; e < kN; e += 2) {
-          const float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nm2);
-          const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          w[e / 2] = pack_bf16x2(pe.x, pe.y);
-          ls2[(e / 2) & 1] = fadd2(ls2[(e / 2) & 1], pe);
-        }
-        l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
-        tmem_st32(s_addr, w);
+        mla_write_p(v, s_addr, sc2, nm2, l);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();

@@ -22,7 +22,9 @@
 //             warps: one thread's tcgen05.mma issue rate and commits limited a
 //             single issuer);
 //   warps 2-5 one query row per thread: one-pass online softmax on S read from
-//             TMEM, P written back over S as bf16 pairs, O rescaled in TMEM
+//             TMEM, P written back over S as bf16 pairs (for items whose rows
+//             see few keys, also their rounding remainders, which enter P V
+//             too), O rescaled in TMEM
 //             only when the running max grows by more than 2^8; an item's
 //             epilogue (O / l, log-sum-exp) runs after the next item's first
 //             tile, a full bf16 O tile staged in the item's Q buffer and
@@ -88,6 +90,17 @@ static_assert(sizeof(BarsT<3, 2, 2>) <= 256 && sizeof(BarsT<2, 3, 2>) <= 256, "b
 struct PItem {
   int r, qt, h, g, q0, rows, qo_len, kv, n_kv, pbase, need;
 };
+
+// Items whose first query row sees fewer keys than this take P to P V in two
+// bf16 parts. Rounding P to bf16 (8 significant bits) moves a row's output by
+// up to a few 1e-3 when a few keys carry the weight, as in the first rows of
+// a causal prefill; over more keys the independent rounding errors of the
+// weights average out.
+constexpr int kSplitBelowKeys = 128;
+__device__ __forceinline__ bool split_item(int causal, int tile_rows, int qt, int qo_len, int kv) {
+  const int first_keys = causal ? min(kv, kv - qo_len + qt * tile_rows + 1) : kv;
+  return first_keys < kSplitBelowKeys;
+}
 
 __device__ __forceinline__ int kv_tiles(int qt, int qo_len, int kv, int causal, int tile_rows) {
   if (kv <= 0) return 0;
@@ -197,6 +210,34 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const TileB
     const int c1 = p.nhd ? g : t.soff, c2 = p.nhd ? t.soff : g;
     tma_load_4d(dst + lane * pb * 128, map, 0, c1, c2, t.pid, bar);
     tma_load_4d(dst + kHalf + lane * pb * 128, map, 64, c1, c2, t.pid, bar);
+  }
+}
+
+// Split items: the rounding remainders bf16(p - bf16(p)) of one row's weights
+// P = 2^(s * scale - m), written to TMEM columns 64 .. 127 of its S buffer
+// (keys 32c .. 32c + 31 in columns 64 + 16c .. 64 + 16c + 15) before the bf16
+// pairs of P overwrite columns 0 .. 63. S is read back from TMEM 32 columns at
+// a time, highest first, so no chunk is overwritten before it is read; keys at
+// or past ncol (masked) get weight 0, as in the pairs. P V adds
+// the product of these remainders to that of the pairs, so it sees p to about
+// 16 bits.
+__device__ __forceinline__ void write_p_remainders(uint32_t s_addr, float2 sc2, float2 nm2, int ncol) {
+#pragma unroll 1
+  for (int c = kBN / 32 - 1; c >= 0; --c) {
+    uint32_t v[32], w[16];
+    tmem_ld32(s_addr + 32 * c, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = 32 * c + e < ncol ? v[e] : 0xff800000u;  // masked keys: weight 0
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nm2);
+      const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+      const uint32_t hi = pack_bf16x2(pe.x, pe.y);
+      const float2 r = ffma2(make_float2(bf16_lo(hi), bf16_hi(hi)), make_float2(-1.f, -1.f), pe);  // exact
+      w[e / 2] = pack_bf16x2(r.x, r.y);
+    }
+    tmem_st16(s_addr + kBN / 2 + 16 * c, w);
   }
 }
 
@@ -445,11 +486,17 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         tc_fence_after();
         if (lane == 0) {
           const uint64_t dv = sw128_desc(sVa + slot * kTileBytes, kHalf, 1024);
-          const uint32_t pa = tmem + col_s(sb);  // P: 64 columns of bf16 pairs
+          const uint32_t pa = tmem + col_s(sb);
+          // P: 64 columns of bf16 pairs; for split items the rounding
+          // remainders follow in the buffer's other 64 columns
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            tc_mma_f16_tmem_a(t_o, pa + 8 * kk, desc_advance(dv, kk * 2048), idesc_pv,
-                              (j > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_f16_tmem_a(t_o, pa + 8 * kk, desc_advance(dv, kk * 2048), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          if (split_item(p.causal, p.tile_rows, I.qt, I.qo_len, I.kv)) {
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              tc_mma_f16_tmem_a(t_o, pa + kBN / 2 + 8 * kk, desc_advance(dv, kk * 2048), idesc_pv, 1u);
+          }
           tc_commit(&bars->pv_done[sb]);  // also frees the S buffer
           tc_commit(&bars->v_empty[slot]);
         }
@@ -575,8 +622,7 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       const int qb = it_ctr % kQB, ob = it_ctr & 1;
       const uint32_t o_addr = t_lane + col_o(ob);
       const int lim = I.kv - I.qo_len + I.qt * p.tile_rows + qrow;  // last key this row may see (causal)
-      // l: sum of the weights (normalises O, gives the lse); P enters P V
-      // rounded to bf16, an unbiased rounding far inside the output tolerance
+      // l: sum of the fp32 weights (normalises O, gives the lse)
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < I.n_kv; ++j) {
         const int sb = s_ctr % kSB;
@@ -645,6 +691,7 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         // P = 2^(s * scale - m) as bf16 pairs, written over the S columns
         // (masked columns: -inf, weight 0). Sums in packed pairs.
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m, -m);
+        if (split_item(p.causal, p.tile_rows, I.qt, I.qo_len, I.kv)) write_p_remainders(s_addr, sc2, nm2, ncol);
         float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         uint32_t w[kBN / 2];
 #pragma unroll

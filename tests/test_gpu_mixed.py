@@ -34,6 +34,8 @@ def check_vs_oracle(case, o, lse, o_tol=1e-2):
 def test_mixed_1p63d_workload_full():
     # one prefill of 1024 tokens + 63 decodes with kv_len U[512, 576], 40 heads, D 128, bf16
     case = wl.mixed_1p_nd()
+    d, ob, lseb = run_mixed(case, torch.bfloat16)   # the call the benchmark times
+    check_vs_oracle(case, ob, lseb)
     d, o, lse = run_mixed(case)
     check_vs_oracle(case, o, lse)
     # the same batch as separate launches: prefill request alone, decodes alone
@@ -65,10 +67,8 @@ def test_mixed_shapes(qo, kv, hq, hkv):
 def test_mixed_bf16_output():
     case = wl.make_attn_case(402, [128, 1, 1, 256], [128, 700, 33, 256], 4, 2, 128, 16, wl.BF16, causal=True)
     _, o, lse = run_mixed(case, torch.bfloat16)
-    o_ref, lse_ref = oracle.attention_case(case)
-    e = np.floor(np.log2(np.maximum(np.abs(o_ref), 2.0 ** -126)))
-    bound = 1e-2 + 2.0 ** (e - 8)
-    assert np.all(np.abs(host_f64(o) - o_ref) <= bound)
+    assert o.dtype == torch.bfloat16
+    check_vs_oracle(case, o, lse)
 
 
 @pytest.mark.parametrize("qo,kv,hq,hkv", [

@@ -2,9 +2,10 @@
 oracle on the same seeded bf16 inputs.
 
 Tolerance stated for this path: max |o - oracle| <= 1e-2 with fp32
-accumulation, |lse - oracle| <= 1e-3. With a bf16 output the stored value is
-additionally rounded to bf16, which alone moves it by up to half a bf16 ulp of
-|o|; the bf16-output checks allow that rounding on top of 1e-2."""
+accumulation, |lse - oracle| <= 1e-3, asserted as is on fp32 and on bf16
+outputs. A bf16 output's own rounding takes up to half a bf16 ulp of |o|
+(7.8e-3 for |o| in [2, 4), which the first rows of a causal prefill reach), so
+the kernel's error before that rounding has to stay near 2e-3."""
 import numpy as np
 import pytest
 import torch
@@ -17,11 +18,6 @@ pytestmark = pytest.mark.gpu
 if torch.cuda.is_available():
     import decode_ragged_paged_gb300 as pd
     from gpu_util import DevCase, LSE_TOL, host_f64
-
-
-def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
-    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
-    return 2.0 ** (e - 8)
 
 
 def run_prefill(case, o_dtype=torch.float32, status=None):
@@ -39,8 +35,7 @@ def check(case, o_dtype=torch.float32, ref=None):
     got = host_f64(o)
     assert np.isfinite(got).all(), "non-finite output"
     err = np.abs(got - o_ref)
-    bound = 1e-2 + (half_ulp_bf16(o_ref) if o_dtype == torch.bfloat16 else 0.0)
-    assert np.all(err <= bound), f"max |o - oracle| = {err.max()} (max allowed {bound.max()})"
+    assert float(err.max()) <= 1e-2, f"max |o - oracle| = {err.max()}"
     lg = lse.cpu().numpy().astype(np.float64)
     fin = np.isfinite(lse_ref)
     assert np.array_equal(np.isfinite(lg), fin)
@@ -53,23 +48,42 @@ def test_prefill_single_tile():
     check(wl.make_attn_case(301, [100], [100], 2, 2, 128, 16, wl.BF16, causal=True, num_pages=8))
 
 
+def _appended(case):
+    """The pools as the append must leave them, written by the oracle's append."""
+    kp, vp = case.k_pool.copy(), case.v_pool.copy()
+    oracle.kv_append(case.qo_indptr, case.kv_len, case.table.page_indptr, case.table.page_indices,
+                     case.k_new, case.v_new, kp, vp)
+    return kp, vp
+
+
 def test_causal_prefill_workload_full():
-    # 8 requests x 512 tokens, 40 = 40 heads, D 128, page 16, bf16; K/V appended first
+    # 8 requests x 512 tokens, 40 = 40 heads, D 128, page 16, bf16; K/V appended
+    # first. The bf16-output call is the one the benchmark times.
     case = wl.causal_prefill()
     d = DevCase(case)
     pd.pd_kv_append(d.k_new, d.v_new, d.k_pool, d.v_pool, d.qo_indptr, d.kv_len, d.page_indptr, d.page_indices,
                     max_kv_len=512)
-    full = wl.make_attn_case(3, [512] * 8, [512] * 8, 40, 40, 128, 16, wl.BF16, causal=True)
-    assert np.array_equal(d.k_pool.view(torch.int16).cpu().numpy().view(np.uint16), full.k_pool)
-    ref = oracle.attention_case(full)
-    o, lse = pd.pd_attn_prefill(d.q, d.k_pool, d.v_pool, d.kv_len, d.page_indptr, d.page_indices, d.qo_indptr,
-                                max_qo_len=512, max_kv_len=512, o_dtype=torch.float32)
-    torch.cuda.synchronize()
-    err = float(np.abs(host_f64(o) - ref[0]).max())
-    lerr = float(np.abs(lse.cpu().numpy() - ref[1]).max())
-    assert err <= 1e-2 and lerr <= LSE_TOL, (err, lerr)
-    # bf16 output of the same call
-    check(full, torch.bfloat16, ref=ref)
+    kp, vp = _appended(case)
+    assert np.array_equal(d.k_pool.view(torch.int16).cpu().numpy().view(np.uint16), kp)
+    assert np.array_equal(d.v_pool.view(torch.int16).cpu().numpy().view(np.uint16), vp)
+    case.k_pool, case.v_pool = kp, vp
+    ref = oracle.attention_case(case)
+    for o_dtype in (torch.bfloat16, torch.float32):
+        o, lse = pd.pd_attn_prefill(d.q, d.k_pool, d.v_pool, d.kv_len, d.page_indptr, d.page_indices, d.qo_indptr,
+                                    max_qo_len=512, max_kv_len=512, o_dtype=o_dtype)
+        torch.cuda.synchronize()
+        assert o.dtype == o_dtype
+        err = float(np.abs(host_f64(o) - ref[0]).max())
+        lerr = float(np.abs(lse.cpu().numpy() - ref[1]).max())
+        assert err <= 1e-2 and lerr <= LSE_TOL, (o_dtype, err, lerr)
+
+
+@pytest.mark.parametrize("seed", [11, 12, 13])
+def test_causal_prefill_workload_other_seeds_bf16_output(seed):
+    # the same shape drawn from other seeds, bf16 output, plain 1e-2
+    case = wl.causal_prefill(seed=seed)
+    case.k_pool, case.v_pool = _appended(case)
+    check(case, torch.bfloat16)
 
 
 @pytest.mark.parametrize("qo,kv,hq,hkv,p,causal", [

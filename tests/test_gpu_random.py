@@ -7,8 +7,7 @@ grouped-query head counts, page size, pool layout and output dtype. Calls with
 many query rows per request and decode-like calls run different shapes of the
 tensor-core kernel, and small batches run short persistent grids; all of them
 must meet the same bars as the fixed cases: |o - oracle| <= 1e-2 for bf16
-inputs (fp32 outputs; a bf16 output also carries its own rounding of half a
-bf16 ulp), 1e-4 for fp32 inputs, |lse - oracle| <= 1e-3."""
+inputs (fp32 or bf16 outputs alike), 1e-4 for fp32 inputs, |lse - oracle| <= 1e-3."""
 import numpy as np
 import pytest
 import torch
@@ -62,11 +61,6 @@ def _case(seed, kind):
     return case, o_dtype
 
 
-def _half_ulp_bf16(x):
-    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
-    return 2.0 ** (e - 8)
-
-
 @pytest.mark.parametrize("kind", ["decode", "prefill", "mixed"])
 @pytest.mark.parametrize("seed", list(range(700, 708)))
 def test_random_batches(kind, seed):
@@ -85,9 +79,8 @@ def test_random_batches(kind, seed):
     got = host_f64(o)
     assert np.isfinite(got).all(), "non-finite output"
     tol = 1e-4 if case.dtype == wl.F32 else 1e-2
-    bound = tol + (_half_ulp_bf16(o_ref) if o_dtype == torch.bfloat16 else 0.0)
     err = np.abs(got - o_ref)
-    assert np.all(err <= bound), f"{kind} seed {seed}: max |o - oracle| = {err.max()}"
+    assert float(err.max()) <= tol, f"{kind} seed {seed}: max |o - oracle| = {err.max()}"
     lg = lse.cpu().numpy().astype(np.float64)
     fin = np.isfinite(lse_ref)
     assert np.array_equal(np.isfinite(lg), fin)
@@ -113,8 +106,7 @@ def test_random_mla_batches(seed):
                                        c.sm_scale)
     got = host_f64(o)
     assert np.isfinite(got).all()
-    bound = 1e-2 + (_half_ulp_bf16(o_ref) if o_dtype == torch.bfloat16 else 0.0)
-    assert np.all(np.abs(got - o_ref) <= bound), f"seed {seed}: max |o - oracle| = {np.abs(got - o_ref).max()}"
+    assert float(np.abs(got - o_ref).max()) <= 1e-2, f"seed {seed}: max |o - oracle| = {np.abs(got - o_ref).max()}"
     lg = lse.cpu().numpy().astype(np.float64)
     fin = np.isfinite(lse_ref)
     assert np.array_equal(np.isfinite(lg), fin)
