@@ -175,26 +175,26 @@ def test_pack_unpack_fp32_odd_pages():
     np.testing.assert_array_equal(buf.cpu().numpy(), ref)
 
 
-def test_handoff_workload_full_sampled():
+def test_handoff_workload_full():
     # 8 requests x 512 tokens x 40 layers x 40 heads x 128, bf16; pages 16 -> 64.
-    # The full round trip is checked on the GPU (pack o unpack o pack); layers
-    # 0, 17 and 39 of every request are checked against the oracle.
-    hc = wl.kv_handoff()
+    # The packed buffer and both destination pools are compared with the
+    # oracle's pack and unpack in full. The destination pool has three pages
+    # per layer that no request owns: they must keep their poison.
+    hc = wl.kv_handoff(dst_slack=3)
     buf, k_dst, v_dst = _handoff_roundtrip(hc)
-    layers = [0, 17, 39]
-    sub = wl.HandoffCase(hc.dtype, len(layers), hc.num_kv_heads, hc.head_dim, hc.kv_len, hc.src_page_size,
-                         hc.src_table, np.ascontiguousarray(hc.k_src[layers]), np.ascontiguousarray(hc.v_src[layers]),
-                         hc.dst_page_size, hc.dst_table, None)
-    per = 2 * hc.num_kv_heads * 512 * hc.head_dim * 2  # bytes of one layer of one request
-    sub_offs = np.arange(8, dtype=np.int64) * per * len(layers)
-    ref = oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, sub.k_src, sub.v_src,
-                         sub_offs, per * len(layers) * 8)
-    host = buf.cpu().numpy()
-    for r in range(8):
-        for j, layer in enumerate(layers):
-            got = host[hc.dst_offsets[r] + layer * per: hc.dst_offsets[r] + (layer + 1) * per]
-            exp = ref[sub_offs[r] + j * per: sub_offs[r] + (j + 1) * per]
-            np.testing.assert_array_equal(got, exp)
+    ref = oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, hc.k_src, hc.v_src,
+                         hc.dst_offsets, buf.numel())
+    assert np.array_equal(buf.cpu().numpy(), ref)
+    shape = tuple(k_dst.shape)
+    k_ref, v_ref = wl._poison(shape, hc.dtype), wl._poison(shape, hc.dtype)
+    oracle.kv_unpack(hc.kv_len, hc.dst_table.page_indptr, hc.dst_table.page_indices, ref, hc.dst_offsets,
+                     k_ref, v_ref)
+    used = np.zeros(hc.dst_table.num_pages, dtype=bool)
+    used[hc.dst_table.page_indices] = True
+    assert not used.all()
+    assert np.all(_host_bits(k_ref)[:, ~used] == wl.BF16_NAN)
+    assert np.array_equal(_bits(k_dst), _host_bits(k_ref))
+    assert np.array_equal(_bits(v_dst), _host_bits(v_ref))
 
 
 def test_pack_bad_offset_is_reported():

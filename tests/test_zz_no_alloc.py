@@ -2,11 +2,14 @@
 workspace from the caller (its scratch is a fixed array inside the library),
 for callers that cannot allocate device memory themselves.
 
-Called through the C ABI and compared with pd_attn_decode on the same inputs,
-on two calls in a row with different batches, so that anything the first call
-left in the shared scratch array would show up in the second. This file is
-collected last so that a run stopping at the first failure has already run
-every other test; it also passes on its own in a fresh process."""
+Called through the C ABI on two batches in a row: a large grouped-query batch
+that runs on the tensor-core kernel, then a smaller one that runs the split-KV
+kernel with its partial results in the array, so that anything the first call
+left in the shared scratch array would show up in the second. Each result must
+be bit-identical to pd_attn_decode with a workspace of its own (the same
+kernels on the same plan) and within the stated tolerances of the fp64 oracle.
+This file is collected last so that a run stopping at the first failure has
+already run every other test; it also passes on its own in a fresh process."""
 import ctypes
 
 import numpy as np
@@ -19,7 +22,8 @@ pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     import decode_ragged_paged_gb300 as pd
-    from gpu_util import DevCase, TOL, LSE_TOL
+    import oracle
+    from gpu_util import DevCase, compare
 
 
 def _static_fn():
@@ -51,16 +55,22 @@ def _case(seed, n, kv_hi, hq=32, hkv=8):
 
 
 def test_static_decode_matches_workspace_decode_twice():
-    cases = [_case(901, 48, 4096), _case(902, 37, 2500, hq=16, hkv=4)]
-    for case in cases:                      # two calls in a row, different batches
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    big = -(-4 * sms // 8) + 8                      # (request, KV head) pairs above 4 per SM
+    cases = [(_case(901, big, 1500), "prefill_kernel"),            # tensor-core path
+             (_case(902, 37, 2500, hq=16, hkv=4), "decode_kernel")]  # split-KV path
+    for case, kernel in cases:              # two calls in a row, different batches and paths
         d = DevCase(case)
         ref_o, ref_lse = pd.pd_attn_decode(d.q, d.k_pool, d.v_pool, d.kv_len, d.page_indptr, d.page_indices,
                                            max_kv_len=d.max_kv_len)
+        torch.cuda.synchronize()
+        assert pd.pd_last_kernel() == kernel
         rc, o, lse, status = _run_static(d, d.max_kv_len)
         assert rc == pd.PD_OK and status == 0
-        err_o = float((o.float() - ref_o.float()).abs().max())
-        err_l = float((lse - ref_lse).abs().max())
-        assert err_o <= TOL[wl.BF16] and err_l <= LSE_TOL, (err_o, err_l)
+        assert pd.pd_last_kernel() == kernel
+        assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+        o_ref, lse_ref = oracle.attention_case(case)
+        compare(o, lse, o_ref, lse_ref, wl.BF16)
 
 
 def test_static_decode_rejects_batch_beyond_scratch():

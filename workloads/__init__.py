@@ -1,9 +1,13 @@
 """Seeded synthetic inputs for the paged-attention and KV-handoff hot path.
 
 This module is shared by the CUDA path's tests and benchmark and by the fp64
-oracle's tests. It only draws random numbers and lays them out: it holds none
-of the method's arithmetic (no dot products, no softmax, no index mapping of
-tokens to page slots beyond choosing which physical pages a request owns).
+oracle's tests. It draws random numbers and lays them out, and holds none of
+the attention arithmetic (no dot products, no softmax, no merge). To place a
+request's tokens and poison the slots that hold none, ``logical_slots`` does
+use the paged cache's token -> (page, slot) map (page t // P of the request's
+page list, slot t % P). The oracle and the CUDA path each compute that map
+themselves, and no test takes an expected value from this module: copies and
+attention outputs are compared with the oracle's results.
 
 Layouts produced here (all C-contiguous numpy arrays):
 
