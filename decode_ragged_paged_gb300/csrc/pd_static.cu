@@ -23,8 +23,10 @@ namespace pd {
 
 namespace {
 
-// Fixed maximum scratch per device. The 128-request decode batch with
-// kv_len up to 4096 and 32 query heads of 128 needs about 17 MiB.
+// Fixed maximum scratch per device. The tensor-core decode path uses a few
+// KiB of it (a header and the work list); the split-KV path keeps its partial
+// results here, about 17 MiB for 128 requests with kv_len up to 4096 and 32
+// query heads of 128.
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;
 
 __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
@@ -36,7 +38,9 @@ void* g_scratch_ptr[kMaxDevices] = {};
 // Device address of this device's copy of the array. In host code
 // g_decode_scratch names a host-side stand-in, not device memory, so the
 // address is looked up through the runtime once per device (with that device
-// current) and cached.
+// current) and cached for the life of the process. A cudaDeviceReset destroys
+// the context the address belongs to; the header tells callers not to use this
+// entry point on a device after resetting it.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;

@@ -185,12 +185,17 @@ PD_API int pd_attn_decode(const pd_attn_desc *desc, const pd_batch *batch, const
  * scratch space is a fixed array of 32 MiB in device memory defined by the
  * library, reserved on every GPU where it is first used until the process
  * exits. A batch whose plan and split-KV partials need more than that returns
- * PD_ERR_WORKSPACE and launches nothing (the 128-request batch with kv_len up to
- * 4096 and 32 query heads of 128 needs about 17 MiB). All calls on one GPU share
- * the array: calls whose work overlaps on the GPU (e.g. on two streams) race
- * and must be serialised by the caller. The first call on each GPU looks up the
- * array's device address through the CUDA runtime (a one-time step that may load
- * the library's device code); make that first call outside any stream capture.
+ * PD_ERR_WORKSPACE and launches nothing. Batches that take the tensor-core
+ * kernel use only a few KiB of the array (a header and the work list); the
+ * split-KV kernel keeps its partial results there, which for 128 requests with
+ * kv_len up to 4096 and 32 query heads of 128 would take about 17 MiB. All
+ * calls on one GPU share the array: calls whose work overlaps on the GPU (e.g.
+ * on two streams) race and must be serialised by the caller. The first call on
+ * each GPU looks up the array's device address through the CUDA runtime (a
+ * one-time step that may load the library's device code) and keeps it for the
+ * life of the process; make that first call outside any stream capture, and do
+ * not use this call on a device after cudaDeviceReset there (the kept address
+ * belonged to the context that the reset destroyed).
  */
 PD_API int pd_attn_decode_static(const pd_attn_desc *desc, const pd_batch *batch, const void *q,
                                  const void *k_pool, const void *v_pool, void *o, float *lse,
