@@ -329,26 +329,67 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (1.14 GB of KV pages); no flush between steps",
-                   "step": "one pd_attn_decode call (this grouped-query batch: plan + tensor-core kernel with the "
-                           "4 query heads of a group packed in one tile)"},
+                   "l2": "inputs larger than L2 (1.14 GB of KV pages); no flush",
+                   "step": "one pd_attn_decode call"},
         "roofline": {"bound": "hbm", "kernel": main_kernel, "achieved": round(achieved, 1),
                      "peak": peaks["hbm"], "unit": "GB/s", "frac": round(achieved / peaks["hbm"], 4),
                      "peak_source": peaks["source"], "traffic": profiled_traffic(main_kernel),
                      "algorithmic_bytes": step_bytes, "kernel_ms": round(kernel_ms, 5)},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
-                "copies": "every step: q and the page tables from one pinned buffer (one H2D copy), o and lse "
-                          "back in one D2H copy; copies on a second stream, double-buffered, so a step's inputs "
-                          "travel while the previous step computes; the host waits for each result one step "
-                          "later; host wall clock",
+                "copies": "per step one pinned H2D (q, tables) and one D2H (o, lse), double-buffered on a "
+                          "copy stream; host wall clock",
                 "results_match_plain_step": e2e_check},
         "gpu_launches": (2 if main_kernel == "prefill_kernel" else 3) * K,  # plan + kernel (+ merge)
         "clocks": clocks,
         "cpu_baseline": cpu,
-        "rows": rows,
+        "rows": compact_rows(rows),
     }
+    if rows:
+        print(json.dumps({"rows_detail": rows}), file=sys.stderr, flush=True)
     print(json.dumps(line), flush=True)
+
+
+def compact_rows(rows: dict) -> dict:
+    """Per row: call ms, kernel ms, and the kernel's fraction of its roofline
+    (hbm: of the measured HBM copy bandwidth; bf16: of the measured bf16 dense
+    peak). The full figures of every row go to stderr as one JSON line."""
+    out = {}
+    for name, r in rows.items():
+        if "status" in r:
+            out[name] = {"err": r["status"][:40]}
+            continue
+        c = {}
+        for src, dst in (("ms", "ms"), ("fused_ms", "ms"), ("kernel_ms", "kms"), ("fused_kernel_ms", "kms"),
+                         ("prefill_kernel_ms", "kms"), ("separate_ms", "sep_ms"), ("decode_only_ms", "dec_ms"),
+                         ("tail_streamed_ms", "tail_ms"), ("tail_after_all_layers_ms", "tail_serial_ms")):
+            if src in r:
+                c[dst] = round(r[src], 4)
+        if "frac_hbm" in r:
+            c["hbm"] = round(r["frac_hbm"], 3)
+        if "frac_bf16" in r:
+            c["bf16"] = round(r["frac_bf16"], 3)
+        if "TFLOPs" in r:
+            c["tf"] = round(r["TFLOPs"])
+        out[name] = c
+    return out
+
+
+def make_flush(dev):
+    """Two 512 MB buffers: one the flush writes, one it then reads."""
+    import torch
+    return (torch.empty(512 << 20, dtype=torch.uint8, device=dev),
+            torch.zeros(64 << 20, dtype=torch.int64, device=dev))
+
+
+def flush_l2(flush) -> None:
+    """Evict L2 between timed calls: write a buffer larger than L2, then read
+    another one. After the write alone the L2 would hold the write's dirty
+    lines, and the timed call would pay their write-back to HBM; after the read
+    it holds clean lines only."""
+    w, r = flush
+    w.zero_()
+    r.sum()
 
 
 def timed(fn, reps, warm, flush=None, prof=True):
@@ -365,7 +406,7 @@ def timed(fn, reps, warm, flush=None, prof=True):
     evs, host = [], []
     for _ in range(reps):
         if flush is not None:
-            flush.zero_()
+            flush_l2(flush)
         a, b, ka, kb = (torch.cuda.Event(enable_timing=True) for _ in range(4))
         if prof:
             ka.record()  # torch creates the CUDA event on its first record
@@ -461,7 +502,7 @@ def measure_rows(args, dev, peaks) -> dict:
 
     rows = {}
     reps, warm = args.row_reps, 3
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = make_flush(dev)
     hbm = peaks["hbm"]
 
     # causal prefill workload: append of its 4096 new tokens, then attention
@@ -758,8 +799,11 @@ def profile_row(name: str, reps: int) -> None:
     import decode_ragged_paged_gb300 as pd
     from workloads import torch_gen
     pd.load_library()
-    if name == "decode":
-        w = torch_gen.decode_batch()
+    if name in ("decode", "decode16"):
+        # decode16: the decode batch's shape with 16 requests (captures beyond
+        # the launch list run on this small case; the tensor-core dispatch needs
+        # 4 (request, KV head) pairs per SM, so it runs the split-KV kernel)
+        w = torch_gen.decode_batch(batch=128 if name == "decode" else 16)
         fn = lambda: pd.pd_attn_decode(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
                                        w["page_indices"], max_kv_len=4096)
     elif name in ("prefill", "append"):
@@ -784,8 +828,10 @@ def profile_row(name: str, reps: int) -> None:
         w = torch_gen.mla_decode_batch()
         fn = lambda: pd.pd_mla_decode(w["q"], w["kv_pool"], w["kv_len"], w["page_indptr"], w["page_indices"],
                                       kv_lora_rank=w["d_c"], sm_scale=192 ** -0.5, max_kv_len=4096)
-    elif name in ("pack", "unpack"):
-        w = torch_gen.kv_handoff()
+    elif name in ("pack", "unpack", "pack2", "unpack2"):
+        # pack2 / unpack2: the handoff with 2 of its 40 layers (small captures)
+        w = torch_gen.kv_handoff(layers=40 if name in ("pack", "unpack") else 2)
+        name = name.rstrip("2")
         if name == "pack":
             fn = lambda: pd.pd_kv_pack(w["k_src"], w["v_src"], w["kv_len"], w["src_indptr"], w["src_indices"],
                                        w["buffer"], w["offsets"], max_kv_len=512)
