@@ -172,29 +172,40 @@ __device__ __forceinline__ bool request_ok(const PrefillParams& p, int r) {
   return code == 0;
 }
 
+// An item's page ids are read 32 at a time: lane l of a producer warp holds
+// the id of page 32 w + l of the request's list (window w; unused past its
+// last page). The read is issued a window (or, for an item's first window, an
+// item) before the ids are needed, so its latency stays off the loads.
+__device__ __forceinline__ int window_pid(const PrefillParams& p, int pbase, int need, int w, int lane) {
+  const int pidx = w * 32 + lane;
+  return pidx < need ? __ldg(p.page_indices + pbase + pidx) : 0;
+}
+
+// Window holding the first page of 128-token tile j (a tile's pages never
+// straddle two windows: a tile spans 128 / page_size pages, a power of two
+// up to 16, or one page).
+__device__ __forceinline__ int tile_window(const PrefillParams& p, int j) { return (j * kBN / p.page_size) >> 5; }
+
 // Boxes of one 128-token K or V tile: per 64-column half, one box per page (or
 // one box of 128 slots when a page holds at least 128 tokens). Lane l < boxes
-// finds its box's page and slot offset; pages past the request's end (and bad
-// ids) map to num_pages, which the TMA unit fetches as zeros.
+// takes its box's page id from the window and its slot offset; pages past the
+// request's end (and bad ids) map to num_pages, which the TMA unit fetches as
+// zeros.
 struct TileBox {
   int pid, soff;
 };
 
-__device__ __forceinline__ TileBox tile_box(const PrefillParams& p, int pbase, int need, int j, int lane) {
+__device__ __forceinline__ TileBox tile_box(const PrefillParams& p, int need, int j, int win_pid, int lane) {
   const int pb = p.page_size < kBN ? p.page_size : kBN;  // slots per box
   const int nb = kBN / pb;                                // boxes per half
-  TileBox t{p.num_pages, 0};
-  if (lane < nb) {
-    const int tok = j * kBN + lane * pb;
-    const int pidx = tok / p.page_size;
-    t.soff = tok % p.page_size;
-    if (pidx < need) {
-      t.pid = __ldg(p.page_indices + pbase + pidx);
-      if (t.pid < 0 || t.pid >= p.num_pages) {
-        report(p.status, PD_DEV_BAD_PAGE_TABLE);
-        t.pid = p.num_pages;
-      }
-    }
+  const int tok = j * kBN + (lane < nb ? lane : 0) * pb;
+  const int pidx = tok / p.page_size;
+  TileBox t{__shfl_sync(0xffffffffu, win_pid, pidx & 31), tok % p.page_size};
+  if (pidx >= need) {
+    t.pid = p.num_pages;
+  } else if (t.pid < 0 || t.pid >= p.num_pages) {
+    if (lane < nb) report(p.status, PD_DEV_BAD_PAGE_TABLE);
+    t.pid = p.num_pages;
   }
   return t;
 }
@@ -367,9 +378,13 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
     const bool is_v = warp == kWarpV;
     uint32_t it_ctr = 0, kv_ctr = 0;
     PItem nxt = prefill_item_or_empty(p, round_item(0), n_items);
+    int pid_first = window_pid(p, nxt.pbase, nxt.need, 0, lane);  // first page-id window of the next item
     for (int it = round_item(0); it < n_items; ++it_ctr, it = round_item(it_ctr)) {
       const PItem I = nxt;
       nxt = prefill_item_or_empty(p, round_item(it_ctr + 1), n_items);
+      int pid_win = pid_first, win = 0;
+      int pid_ahead = window_pid(p, I.pbase, I.need, 1, lane);
+      pid_first = window_pid(p, nxt.pbase, nxt.need, 0, lane);
       if (!is_v) {
         const int qb = it_ctr % kQB;
         if (!warp_mbar_wait(&bars->q_empty[qb], ((it_ctr / kQB) & 1u) ^ 1u, abort, p.status)) break;
@@ -384,7 +399,13 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
       const uint32_t depth = is_v ? (uint32_t)kVSlots : (uint32_t)kKSlots;
       for (int j = 0; j < I.n_kv && ok; ++j, ++kv_ctr) {
         const int slot = kv_ctr % depth;
-        const TileBox box = tile_box(p, I.pbase, I.need, j, lane);  // page ids read before the slot wait
+        const int w = tile_window(p, j);
+        if (w != win) {  // the window read ahead; read the one after it
+          pid_win = pid_ahead;
+          win = w;
+          pid_ahead = window_pid(p, I.pbase, I.need, w + 1, lane);
+        }
+        const TileBox box = tile_box(p, I.need, j, pid_win, lane);
         // A K slot is free again once the S product of its previous tile has
         // completed (k_empty); a V slot once the P V product of its previous
         // tile has (v_empty).
