@@ -668,60 +668,81 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
 #pragma unroll
           for (int e = 0; e < kBN; ++e) v[e] = e < ncol ? v[e] : 0xff800000u;
         }
-        // row max of the tile (four independent chains)
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int e = 0; e < kBN; e += 2)
-          mx[(e / 2) & 3] = fmax3(mx[(e / 2) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        float m_new = m;
-        bool rescale = false;
-        if (mt > -INFINITY) {
-          const float ms = mt * p.scale_log2;
-          if (m == -INFINITY) {
-            m_new = ms;
-          } else if (ms > m + kRescaleThreshold) {
-            m_new = ms;
-            rescale = true;
-          }
-        }
-        // tcgen05.ld / st are warp-collective: the whole warp rescales its rows of
-        // O when any of them needs it (factor 1 for the others), after the
-        // previous P V product has completed. That product's barrier (buffer of
-        // tile s_ctr - 1) cannot move past this phase before this tile's P is
-        // published, so waiting only when needed keeps the phase count exact.
-        if (__any_sync(0xffffffffu, rescale)) {
-          const uint32_t prev = s_ctr - 1;
-          ok = warp_mbar_wait(&bars->pv_done[prev % kSB], (prev / kSB) & 1u, abort, p.status);
-          if (!ok) break;
-          tc_fence_after();
-          const float alpha = rescale ? exp2f(m - m_new) : 1.0f;
-          l *= alpha;
-#pragma unroll
-          for (int c = 0; c < kD / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(o_addr + c * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(o_addr + c * 32, o);
-          }
-          tmem_wait_st();
-        }
-        m = m_new;
         // P = 2^(s * scale - m) as bf16 pairs, written over the S columns
-        // (masked columns: -inf, weight 0). Sums in packed pairs.
-        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m, -m);
-        if (split_item(p.causal, p.tile_rows, I.qt, I.qo_len, I.kv)) write_p_remainders(s_addr, sc2, nm2, ncol);
-        float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        // (masked columns: -inf, weight 0), sums in packed pairs. Once a
+        // warp's rows all have a finite running max m, a tile's P is computed
+        // with that m at once, and the largest exponent is checked in the
+        // same loop: only if some weight would pass 2^kRescaleThreshold is the
+        // tile redone with its exact row max (then O is rescaled). The first
+        // tile of an item, and split items (whose remainder pass reads S from
+        // tensor memory, where the pairs are written), take the exact max
+        // first.
+        const bool split = split_item(p.causal, p.tile_rows, I.qt, I.qo_len, I.kv);
+        bool spec = !split && __all_sync(0xffffffffu, m > -INFINITY);
         uint32_t w[kBN / 2];
+        float2 ls2[2];
+        for (;;) {
+          float m_new = m;
+          bool rescale = false;
+          if (!spec) {
+            // row max of the tile (four independent chains)
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int e = 0; e < kBN; e += 2) {
-          const float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nm2);
-          const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          w[e / 2] = pack_bf16x2(pe.x, pe.y);
-          ls2[(e / 2) & 1] = fadd2(ls2[(e / 2) & 1], pe);
+            for (int e = 0; e < kBN; e += 2)
+              mx[(e / 2) & 3] = fmax3(mx[(e / 2) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            if (mt > -INFINITY) {
+              const float ms = mt * p.scale_log2;
+              if (m == -INFINITY) {
+                m_new = ms;
+              } else if (ms > m + kRescaleThreshold) {
+                m_new = ms;
+                rescale = true;
+              }
+            }
+            // tcgen05.ld / st are warp-collective: the whole warp rescales its
+            // rows of O when any of them needs it (factor 1 for the others),
+            // after the previous P V product has completed. That product's
+            // barrier (buffer of tile s_ctr - 1) cannot move past this phase
+            // before this tile's P is published, so waiting only when needed
+            // keeps the phase count exact.
+            if (__any_sync(0xffffffffu, rescale)) {
+              const uint32_t prev = s_ctr - 1;
+              ok = warp_mbar_wait(&bars->pv_done[prev % kSB], (prev / kSB) & 1u, abort, p.status);
+              if (!ok) break;
+              tc_fence_after();
+              const float alpha = rescale ? exp2f(m - m_new) : 1.0f;
+              l *= alpha;
+#pragma unroll
+              for (int c = 0; c < kD / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(o_addr + c * 32, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                tmem_st32(o_addr + c * 32, o);
+              }
+              tmem_wait_st();
+            }
+            m = m_new;
+          }
+          const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m, -m);
+          if (split) write_p_remainders(s_addr, sc2, nm2, ncol);
+          ls2[0] = make_float2(0.f, 0.f);
+          ls2[1] = make_float2(0.f, 0.f);
+          float xm = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < kBN; e += 2) {
+            const float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nm2);
+            if (spec) xm = fmax3(xm, x.x, x.y);
+            const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            w[e / 2] = pack_bf16x2(pe.x, pe.y);
+            ls2[(e / 2) & 1] = fadd2(ls2[(e / 2) & 1], pe);
+          }
+          if (!spec || !__any_sync(0xffffffffu, xm > kRescaleThreshold)) break;
+          spec = false;  // a weight above 2^8: redo the tile with its exact max
         }
+        if (!ok) break;
         l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
         tmem_st32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(w + 0));
         tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(w + 32));
