@@ -58,6 +58,7 @@ __device__ __forceinline__ uint32_t col_s(int b) { return (uint32_t)b * 128; }
 __device__ __forceinline__ uint32_t col_o(int b) { return (uint32_t)(kSB + b) * 128; }
 static_assert((kSB + 2) * 128 <= 512, "TMEM columns");
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
+constexpr float kSpecSumLimit = 256.0f;        // 2^kRescaleThreshold
 constexpr int kBuckets = 1024;
 
 // Shared memory (offsets from a 1024-byte aligned base): QB Q buffers, then a
@@ -222,6 +223,13 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& p, const TileB
     tma_load_4d(dst + lane * pb * 128, map, 0, c1, c2, t.pid, bar);
     tma_load_4d(dst + kHalf + lane * pb * 128, map, 64, c1, c2, t.pid, bar);
   }
+}
+
+// bf16 pair of two accumulator words (fp32 bits) times a factor, with one
+// packed multiply.
+__device__ __forceinline__ uint32_t scale_pack(const uint32_t* v, float2 f2) {
+  const float2 q = fmul2(make_float2(__uint_as_float(v[0]), __uint_as_float(v[1])), f2);
+  return pack_bf16x2(q.x, q.y);
 }
 
 // Split items: the rounding remainders bf16(p - bf16(p)) of one row's weights
@@ -568,6 +576,7 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         tc_fence_after();
       }
       const float inv_l = E.l > 0.f ? 1.0f / E.l : 0.f;
+      const float2 il2 = make_float2(inv_l, inv_l);
       const bool store = qrow < E.rows;
       const int64_t orow = ((int64_t)(E.q0 + qrow) * p.hq + E.h + qhead) * kD;
       const uint32_t o_addr = t_lane + col_o(E.ob);
@@ -591,10 +600,10 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         const uint32_t so = smem_u32(sO);
 #pragma unroll
         for (int k = 0; k < kD / 8; ++k) {
-          const uint32_t a0 = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l);
-          const uint32_t a1 = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l);
-          const uint32_t a2 = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l);
-          const uint32_t a3 = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l);
+          const uint32_t a0 = scale_pack(v + 8 * k + 0, il2);
+          const uint32_t a1 = scale_pack(v + 8 * k + 2, il2);
+          const uint32_t a2 = scale_pack(v + 8 * k + 4, il2);
+          const uint32_t a3 = scale_pack(v + 8 * k + 6, il2);
           const uint32_t addr = so + (k / 8) * kHalf + row * 128 + (((k % 8) ^ (row & 7)) * 16);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a0), "r"(a1), "r"(a2), "r"(a3)
                        : "memory");
@@ -616,10 +625,10 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
 #pragma unroll
           for (int k = 0; k < kD / 8; ++k) {
             uint4 u;
-            u.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l);
-            u.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l);
-            u.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l);
-            u.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l);
+            u.x = scale_pack(v + 8 * k + 0, il2);
+            u.y = scale_pack(v + 8 * k + 2, il2);
+            u.z = scale_pack(v + 8 * k + 4, il2);
+            u.w = scale_pack(v + 8 * k + 6, il2);
             dst[k] = u;
           }
         } else {
@@ -671,9 +680,12 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
         // P = 2^(s * scale - m) as bf16 pairs, written over the S columns
         // (masked columns: -inf, weight 0), sums in packed pairs. Once a
         // warp's rows all have a finite running max m, a tile's P is computed
-        // with that m at once, and the largest exponent is checked in the
-        // same loop: only if some weight would pass 2^kRescaleThreshold is the
-        // tile redone with its exact row max (then O is rescaled). The first
+        // with that m at once and accepted if the row's weights sum to at most
+        // 2^kRescaleThreshold, which bounds every weight by it; otherwise the
+        // tile is redone with its exact row max (then O is rescaled). The
+        // check costs one comparison per row where a running maximum of the
+        // exponents would cost an instruction per pair of weights, and the
+        // softmax warps are bound by the instructions they issue. The first
         // tile of an item, and split items (whose remainder pass reads S from
         // tensor memory, where the pairs are written), take the exact max
         // first.
@@ -730,17 +742,15 @@ __global__ void __launch_bounds__(kThreadsPf, 1)
           if (split) write_p_remainders(s_addr, sc2, nm2, ncol);
           ls2[0] = make_float2(0.f, 0.f);
           ls2[1] = make_float2(0.f, 0.f);
-          float xm = -INFINITY;
 #pragma unroll
           for (int e = 0; e < kBN; e += 2) {
             const float2 x = ffma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2, nm2);
-            if (spec) xm = fmax3(xm, x.x, x.y);
             const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
             w[e / 2] = pack_bf16x2(pe.x, pe.y);
             ls2[(e / 2) & 1] = fadd2(ls2[(e / 2) & 1], pe);
           }
-          if (!spec || !__any_sync(0xffffffffu, xm > kRescaleThreshold)) break;
-          spec = false;  // a weight above 2^8: redo the tile with its exact max
+          if (!spec || !__any_sync(0xffffffffu, (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y) > kSpecSumLimit)) break;
+          spec = false;  // a weight may pass 2^8: redo the tile with its exact max
         }
         if (!ok) break;
         l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
