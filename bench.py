@@ -825,6 +825,12 @@ def profile_row(name: str, reps: int) -> None:
         else:
             fn = lambda: pd.pd_kv_append(w["k_new"], w["v_new"], w["k_pool"], w["v_pool"], w["qo_indptr"],
                                          w["kv_len"], w["page_indptr"], w["page_indices"], max_kv_len=512)
+    elif name == "prefill_long_small":
+        # a reduced compute-bound causal prefill (1 x 4096, 8 heads: 3.4e10 flop
+        # over 34 MB, 1024 flop/B), for the tensor-pipe counters of a small capture
+        w = torch_gen.paged_batch(3, [4096], [4096], 8, 8, 128, 16)
+        fn = lambda: pd.pd_attn_prefill(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
+                                        w["page_indices"], w["qo_indptr"], max_qo_len=4096, max_kv_len=4096)
     elif name == "decode_mha":
         # the mixed workload's 63 decode requests (40 = 40 heads): the split-KV kernel
         w = torch_gen.mixed_1p_nd()
@@ -867,7 +873,7 @@ def main():
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile-row", default=None,
-                    help="run only this row's call (decode, decode_mha, append, prefill, mixed, mla_decode, pack, "
+                    help="run only this row's call (decode, decode_mha, append, prefill, prefill_long_small, mixed, mla_decode, pack, "
                          "unpack) for ncu")
     ap.add_argument("--profile-reps", type=int, default=3)
     args = ap.parse_args()
