@@ -362,6 +362,7 @@ def compact_rows(rows: dict) -> dict:
         c = {}
         for src, dst in (("ms", "ms"), ("fused_ms", "ms"), ("kernel_ms", "kms"), ("fused_kernel_ms", "kms"),
                          ("prefill_kernel_ms", "kms"), ("separate_ms", "sep_ms"), ("decode_only_ms", "dec_ms"),
+                         ("split_ms", "split_ms"), ("split_frac_hbm", "split_hbm"),
                          ("tail_streamed_ms", "tail_ms"), ("tail_after_all_layers_ms", "tail_serial_ms")):
             if src in r:
                 c[dst] = round(r[src], 4)
@@ -601,6 +602,12 @@ def measure_rows(args, dev, peaks) -> dict:
                               w["page_indices"], max_kv_len=576, o=o_d)
 
         sep_ms, _, _ = timed(separate, reps, warm, flush, prof=False)
+        # the same batch through pd_attn_mixed_split: request 0 is the prefill,
+        # the rest decodes; the two parts at once on disjoint SM partitions
+        split_ms, _, _ = timed(lambda: pd.pd_attn_mixed_split(w["q"], w["k_pool"], w["v_pool"], w["kv_len"],
+                                                               w["page_indptr"], w["page_indices"], w["qo_indptr"],
+                                                               1, max_qo_len=1024, max_kv_len=1024, o=o),
+                               reps, warm, flush, prof=False)
         dec_ms, dec_kms, _ = timed(lambda: pd.pd_attn_decode(w["q"][pre:], w["k_pool"], w["v_pool"], w["kv_len"][1:],
                                                           w["page_indptr"][1:], w["page_indices"], max_kv_len=576,
                                                           o=o_d), reps, warm, flush)
@@ -610,6 +617,9 @@ def measure_rows(args, dev, peaks) -> dict:
                          "GBs": round(kvb / kms / 1e6, 1), "frac_hbm": round(kvb / kms / 1e6 / hbm, 4),
                          "TFLOPs": round(mflops / kms / 1e9, 1), "bound": "hbm", "bytes": kvb, "flops": mflops,
                          "separate_ms": round(sep_ms, 5), "decode_only_ms": round(dec_ms, 5),
+                         "split_ms": round(split_ms, 5), "split_GBs": round(kvb / split_ms / 1e6, 1),
+                         "split_frac_hbm": round(kvb / split_ms / 1e6 / hbm, 4),
+                         "interference_split_over_decode_only": round(split_ms / dec_ms, 3),
                          "decode_only_GBs": round(dec_kvb / dec_kms / 1e6, 1),
                          "interference_fused_over_decode_only": round(ms / dec_ms, 3),
                          "interference_separate_over_decode_only": round(sep_ms / dec_ms, 3)}

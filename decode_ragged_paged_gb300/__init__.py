@@ -29,13 +29,13 @@ LIB_PATH = os.path.join(_HERE, "libpd.so")
 PD_OK, PD_ERR_INVALID_ARG, PD_ERR_UNSUPPORTED, PD_ERR_WORKSPACE, PD_ERR_CUDA, PD_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 PD_F32, PD_BF16 = 0, 1
 PD_LAYOUT_HND, PD_LAYOUT_NHD = 0, 1
-PD_KIND_DECODE, PD_KIND_PREFILL, PD_KIND_MIXED = 0, 1, 2
+PD_KIND_DECODE, PD_KIND_PREFILL, PD_KIND_MIXED, PD_KIND_MIXED_SPLIT = 0, 1, 2, 3
 DEVICE_STATUS = {0: "ok", 1: "bad indptr", 2: "bad length", 3: "bad page table", 4: "not a decode",
                  5: "timeout", 6: "bad offset"}
 
 # Every symbol include/pd.h declares.
 EXPORTS = ("pd_attn_workspace_size", "pd_attn_decode", "pd_attn_decode_static", "pd_attn_prefill",
-           "pd_attn_mixed", "pd_mla_workspace_size", "pd_mla_decode",
+           "pd_attn_mixed", "pd_attn_mixed_split", "pd_mla_workspace_size", "pd_mla_decode",
            "pd_kv_append", "pd_kv_pack", "pd_kv_unpack", "pd_kv_pack_heads", "pd_kv_unpack_heads",
            "pd_kv_pack_layers", "pd_counter_alloc", "pd_counter_free", "pd_layer_signal",
            "pd_messenger_start_pack", "pd_messenger_join",
@@ -93,6 +93,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             for name in ("pd_attn_decode", "pd_attn_prefill", "pd_attn_mixed"):
                 getattr(lib, name).argtypes = attn
                 getattr(lib, name).restype = ctypes.c_int
+            lib.pd_attn_mixed_split.argtypes = attn[:2] + [I32, I32] + attn[2:]
+            lib.pd_attn_mixed_split.restype = ctypes.c_int
             lib.pd_attn_workspace_size.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(Batch), I32]
             lib.pd_attn_workspace_size.restype = S
             lib.pd_mla_workspace_size.argtypes = [ctypes.POINTER(MlaDesc), ctypes.POINTER(Batch)]
@@ -265,6 +267,37 @@ def pd_attn_mixed(q, k_pool, v_pool, kv_len, page_indptr, page_indices, qo_indpt
                  qo_indptr, causal=causal, sm_scale=sm_scale, max_qo_len=max_qo_len, max_kv_len=max_kv_len,
                  o=o, lse=lse, o_dtype=o_dtype, workspace=workspace, dev_status=dev_status, stream=stream,
                  layout=layout)
+
+
+def pd_attn_mixed_split(q, k_pool, v_pool, kv_len, page_indptr, page_indices, qo_indptr, num_prefill, *,
+                        prefill_sms=0, causal=True, sm_scale=None, max_qo_len=None, max_kv_len=None, o=None,
+                        lse=True, o_dtype=None, workspace=None, dev_status=None, stream=None, layout="HND"):
+    """Mixed batch with requests [0, num_prefill) prefill and the rest decode (qo_len 1),
+    the two parts run at the same time on disjoint SM partitions. Returns (o, lse)."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool")):
+        if not t.is_cuda or not t.is_contiguous():
+            raise PdError(f"{n} must be a contiguous CUDA tensor")
+    if max_qo_len is None:
+        max_qo_len = int((qo_indptr[1:] - qo_indptr[:-1]).max().item()) if qo_indptr.numel() > 1 else 0
+    desc = make_attn_desc(q, k_pool, causal=causal, sm_scale=sm_scale, o_dtype=o_dtype, layout=layout)
+    batch = make_batch(kv_len, page_indptr, page_indices, k_pool.shape[0], qo_indptr=qo_indptr,
+                       total_qo=q.shape[0], max_qo_len=max_qo_len, max_kv_len=max_kv_len)
+    if o is None:
+        o = torch.empty(q.shape, dtype=o_dtype if o_dtype is not None else q.dtype, device=q.device)
+    if lse is True:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    elif lse is False:
+        lse = None
+    dref, bref = ctypes.byref(desc), ctypes.byref(batch)
+    if workspace is None or workspace.numel() < pd_attn_workspace_size(desc, batch, PD_KIND_MIXED_SPLIT):
+        workspace = torch.empty(max(pd_attn_workspace_size(desc, batch, PD_KIND_MIXED_SPLIT), 16), dtype=torch.uint8,
+                                device=q.device)
+    rc = lib.pd_attn_mixed_split(dref, bref, int(num_prefill), int(prefill_sms), _ptr(q), _ptr(k_pool),
+                                 _ptr(v_pool), _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                 _ptr(dev_status), _stream(stream, q.get_device()))
+    _check(rc, "pd_attn_mixed_split")
+    return o, lse
 
 
 def pd_mla_decode(q, kv_pool, kv_len, page_indptr, page_indices, *, kv_lora_rank=512, sm_scale=None,

@@ -10,7 +10,13 @@
 
 namespace pd {
 
+int& partition_sms() {
+  static thread_local int n = 0;
+  return n;
+}
+
 int device_sm_count() {
+  if (partition_sms() > 0) return partition_sms();
   static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -86,6 +92,19 @@ DecodeLayout decode_layout_for(const pd_attn_desc* d, const pd_batch* b) {
 }
 
 }  // namespace
+
+// pd_attn_mixed_split's workspace: the prefill part's plan, then the decode
+// part's plan and partials, each sized for the whole batch (the decode part's
+// chunking for all of the device's SMs, the most it uses on a partition).
+MixedSplitLayout mixed_split_layout(const pd_attn_desc* d, const pd_batch* b) {
+  MixedSplitLayout L{};
+  L.decode = align_up(prefill_layout(b->batch_size, b->total_qo, b->max_qo_len,
+                                     prefill_tile_heads(d->num_qo_heads / d->num_kv_heads))
+                          .total,
+                      256);
+  L.total = L.decode + decode_layout_for(d, b).total;
+  return L;
+}
 
 // Plans and launches the tensor-core kernel; arguments already validated.
 int run_prefill(const pd_attn_desc* desc, const pd_batch* batch, int32_t max_qo_len, int32_t causal, const void* q,
@@ -179,6 +198,7 @@ size_t pd_attn_workspace_size(const pd_attn_desc* desc, const pd_batch* batch, i
     return prefill_layout(batch->batch_size, batch->total_qo, batch->max_qo_len,
                           prefill_tile_heads(desc->num_qo_heads / desc->num_kv_heads))
         .total;
+  if (kind == PD_KIND_MIXED_SPLIT) return pd::mixed_split_layout(desc, batch).total;
   return 0;
 }
 

@@ -722,7 +722,7 @@ int run_decode(DecodeParams& p, cudaStream_t stream) {
   static std::atomic<int> configured[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;
-  const bool cached = dev >= 0 && dev < 64;
+  const bool cached = dev >= 0 && dev < 64 && partition_sms() == 0;
   int blocks_per_sm = cached ? configured[dev].load(std::memory_order_acquire) - 1 : 0;
   if (blocks_per_sm < 1) {
     if (cudaFuncSetAttribute(decode_kernel<ES, D, GS>, cudaFuncAttributeMaxDynamicSharedMemorySize,

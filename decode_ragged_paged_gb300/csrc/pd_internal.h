@@ -94,6 +94,13 @@ struct PrefillLayout {
 int32_t prefill_tile_heads(int32_t group);
 PrefillLayout prefill_layout(int32_t batch, int32_t total_qo, int32_t max_qo_len, int32_t tile_heads);
 
+// Workspace of pd_attn_mixed_split: the prefill part at 0, the decode part at
+// `decode` (bytes).
+struct MixedSplitLayout {
+  size_t decode, total;
+};
+MixedSplitLayout mixed_split_layout(const pd_attn_desc* d, const pd_batch* b);
+
 // Checks what the tensor-core prefill supports; returns a pd_status.
 int prefill_supported(int32_t kv_dtype, int32_t head_dim, int32_t page_size);
 
@@ -169,7 +176,13 @@ bool make_rows_map(CUtensorMap* map, const void* base, int32_t dtype, int32_t to
                    int32_t box_cols, int32_t box_rows, bool swizzle128, int32_t box_heads = 1);
 
 // ------------------------------------------------------------------- misc
+// SMs of the device, or of the SM partition (green context) the calling thread
+// launches into while partition_sms() is set.
 int device_sm_count();
+// Set (thread-local) while a call launches into an SM partition: grids are
+// sized for the partition's SMs, and the kernels' one-time attribute setup,
+// which is per context, runs again.
+int& partition_sms();
 
 // Events of pd_profile_events() (per host thread); recorded around main kernels.
 struct ProfileEvents {

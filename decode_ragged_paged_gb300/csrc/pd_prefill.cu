@@ -858,7 +858,7 @@ int launch_prefill(PrefillParams& p, const void* q, const void* k_pool, const vo
   static std::atomic<bool> configured[64][2];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;
-  const bool cached = dev >= 0 && dev < 64;
+  const bool cached = dev >= 0 && dev < 64 && partition_sms() == 0;
   if (!cached || !configured[dev][long_q].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrefillSmem) != cudaSuccess)
       return PD_ERR_CUDA;

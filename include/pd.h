@@ -102,7 +102,7 @@ typedef enum { PD_F32 = 0, PD_BF16 = 1 } pd_dtype;
 
 typedef enum { PD_LAYOUT_HND = 0, PD_LAYOUT_NHD = 1 } pd_layout;
 
-typedef enum { PD_KIND_DECODE = 0, PD_KIND_PREFILL = 1, PD_KIND_MIXED = 2 } pd_attn_kind;
+typedef enum { PD_KIND_DECODE = 0, PD_KIND_PREFILL = 1, PD_KIND_MIXED = 2, PD_KIND_MIXED_SPLIT = 3 } pd_attn_kind;
 
 /* Shape and numerics of one attention call. */
 typedef struct {
@@ -225,6 +225,31 @@ PD_API int pd_attn_prefill(const pd_attn_desc *desc, const pd_batch *batch, cons
 PD_API int pd_attn_mixed(const pd_attn_desc *desc, const pd_batch *batch, const void *q,
                   const void *k_pool, const void *v_pool, void *o, float *lse,
                   void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * Mixed batch whose prefill and decode requests the caller has separated, as
+ * a serving loop that piggybacks prefill chunks on a decode batch knows them
+ * (section "Prefill vs Decode performance"): requests [0, num_prefill) are
+ * prefill requests (any qo_len), requests [num_prefill, B) decode requests
+ * (qo_len = 1; any other length is reported as PD_DEV_NOT_DECODE). The two
+ * parts run at the same time on disjoint sets of SMs (green contexts): the
+ * prefill part on the tensor-core kernel over prefill_sms SMs (0: sized from
+ * the batch's host-side bounds; rounded to the partition granularity of 8),
+ * the decode part on the split-KV kernel over the rest. The call orders both
+ * after the work already queued on `stream` and makes `stream` wait for both.
+ * Where green contexts cannot be created, or one part is empty, it runs as
+ * pd_attn_mixed (or the one part) on `stream`.
+ * Arguments and layouts as pd_attn_mixed; batch->qo_indptr is required; the
+ * workspace is that of pd_attn_workspace_size(kind = PD_KIND_MIXED_SPLIT).
+ * Host-side state: one pair of green contexts with a stream and two events
+ * each per device and partition size, created on first use and kept for the
+ * life of the process (not valid after cudaDeviceReset); calls on one device
+ * are serialised on the host while they enqueue.
+ */
+PD_API int pd_attn_mixed_split(const pd_attn_desc *desc, const pd_batch *batch, int32_t num_prefill,
+                               int32_t prefill_sms, const void *q, const void *k_pool, const void *v_pool,
+                               void *o, float *lse, void *workspace, size_t workspace_bytes,
+                               int32_t *dev_status, void *stream);
 
 /*
  * MLA decode (section "Disaggregated Deployments", "DeepSeek-R1": multi-head
