@@ -205,3 +205,30 @@ def test_mla_workspace_and_pointer_checks(lib):
                              None) == pd.PD_ERR_INVALID_ARG
     assert lib.pd_mla_decode(ctypes.byref(d), ctypes.byref(_batch(batch_size=0)), None, None, None, None, None, 0,
                              None, None) == pd.PD_OK
+
+
+def _split(lib, d, b, num_prefill, prefill_sms=0, ws_bytes=1 << 30):
+    return lib.pd_attn_mixed_split(ctypes.byref(d), ctypes.byref(b), num_prefill, prefill_sms, 16, 16, 16, 16,
+                                   None, 16, ws_bytes, None, None)
+
+
+def test_mixed_split_rejects_bad_arguments(lib):
+    d = _desc()
+    b = _batch(batch_size=3, total_qo=130, max_qo_len=128, max_kv_len=512)
+    assert _split(lib, d, b, 4) == pd.PD_ERR_INVALID_ARG          # more prefill requests than requests
+    assert _split(lib, d, b, -1) == pd.PD_ERR_INVALID_ARG
+    assert _split(lib, d, b, 1, prefill_sms=-8) == pd.PD_ERR_INVALID_ARG
+    assert _split(lib, d, _batch(batch_size=3, qo_indptr=None, total_qo=130, max_qo_len=128, max_kv_len=512),
+                  1) == pd.PD_ERR_INVALID_ARG                    # the split needs qo_indptr
+    assert _split(lib, d, _batch(batch_size=3, total_qo=1, max_qo_len=1, max_kv_len=512),
+                  0) == pd.PD_ERR_INVALID_ARG                    # fewer rows than decode requests
+    assert _split(lib, _desc(num_kv_heads=3), b, 1) == pd.PD_ERR_INVALID_ARG
+    assert _split(lib, d, b, 1, ws_bytes=64) == pd.PD_ERR_WORKSPACE
+
+
+def test_mixed_split_workspace_covers_both_parts(lib):
+    d = _desc()
+    b = _batch(batch_size=64, total_qo=1087, max_qo_len=1024, max_kv_len=1024)
+    sizes = [lib.pd_attn_workspace_size(ctypes.byref(d), ctypes.byref(b), k) for k in range(4)]
+    assert all(s > 0 for s in sizes)
+    assert sizes[pd.PD_KIND_MIXED_SPLIT] >= sizes[pd.PD_KIND_PREFILL] + sizes[pd.PD_KIND_DECODE]
