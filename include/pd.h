@@ -242,9 +242,11 @@ PD_API int pd_attn_mixed(const pd_attn_desc *desc, const pd_batch *batch, const 
  * Arguments and layouts as pd_attn_mixed; batch->qo_indptr is required; the
  * workspace is that of pd_attn_workspace_size(kind = PD_KIND_MIXED_SPLIT).
  * Host-side state: one pair of green contexts with a stream and two events
- * each per device and partition size, created on first use and kept for the
- * life of the process (not valid after cudaDeviceReset); calls on one device
- * are serialised on the host while they enqueue.
+ * each per device and partition size (at most one pair per multiple of 8
+ * SMs), created on first use and kept for the life of the process (not valid
+ * after cudaDeviceReset); calls on one device are serialised on the host while
+ * they enqueue. The parts run on the green contexts' own streams, so the call
+ * cannot be recorded by stream capture into a CUDA graph on `stream`.
  */
 PD_API int pd_attn_mixed_split(const pd_attn_desc *desc, const pd_batch *batch, int32_t num_prefill,
                                int32_t prefill_sms, const void *q, const void *k_pool, const void *v_pool,
