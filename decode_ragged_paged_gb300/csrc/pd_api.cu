@@ -94,15 +94,20 @@ DecodeLayout decode_layout_for(const pd_attn_desc* d, const pd_batch* b) {
 }  // namespace
 
 // pd_attn_mixed_split's workspace: the prefill part's plan, then the decode
-// part's plan and partials, each sized for the whole batch (the decode part's
-// chunking for all of the device's SMs, the most it uses on a partition).
+// part's plan and partials, each sized for the whole batch. The decode part's
+// chunk length depends on the SMs of its partition and on how many requests
+// it gets; sized for the shortest chunk the plan ever picks (an SM count so
+// large that the length sits at its lower bound), it holds any of them.
 MixedSplitLayout mixed_split_layout(const pd_attn_desc* d, const pd_batch* b) {
   MixedSplitLayout L{};
   L.decode = align_up(prefill_layout(b->batch_size, b->total_qo, b->max_qo_len,
                                      prefill_tile_heads(d->num_qo_heads / d->num_kv_heads))
                           .total,
                       256);
-  L.total = L.decode + decode_layout_for(d, b).total;
+  const int gs = decode_heads_per_item(d->num_qo_heads / d->num_kv_heads, d->head_dim);
+  L.total = L.decode + decode_layout(b->batch_size, d->num_qo_heads, d->head_dim, b->max_kv_len,
+                                     d->num_qo_heads / gs, 1 << 20)
+                           .total;
   return L;
 }
 
