@@ -17,6 +17,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <stdlib.h>
+
 #include <map>
 #include <mutex>
 
@@ -125,6 +127,22 @@ GreenPair* green_pair(int dev, int first_sms) {
   return g->ok ? g : nullptr;
 }
 
+// A CUDA tool injected into the process (a profiler or a sanitizer) may not
+// follow launches into green contexts: Nsight Compute stops the application at
+// the first of them. Such tools announce themselves in the environment they
+// give the process: the CUDA injection path, or Nsight's own injection and
+// launch variables.
+bool tool_attached() {
+  static const bool attached = [] {
+    const char* names[] = {"CUDA_INJECTION64_PATH", "NV_NSIGHT_INJECTION_TRANSPORT_TYPE",
+                           "NV_COMPUTE_PROFILER_PERFWORKS_DIR", "NV_TPS_LAUNCH_TOKEN"};
+    for (const char* n : names)
+      if (getenv(n) != nullptr) return true;
+    return false;
+  }();
+  return attached;
+}
+
 // SMs for the prefill part when the caller gives none: enough for it to finish
 // in about the time the decode part takes, from the host-side bounds. The
 // decode part is bound by HBM (about 6 TB/s on the split-KV kernel) and its
@@ -177,7 +195,7 @@ extern "C" int pd_attn_mixed_split(const pd_attn_desc* desc, const pd_batch* bat
   if (first > sms - 8) first = (sms - 8) / 8 * 8;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;
-  GreenPair* g = first >= 8 ? green_pair(dev, first) : nullptr;
+  GreenPair* g = first >= 8 && !tool_attached() ? green_pair(dev, first) : nullptr;
   if (g == nullptr)
     return pd_attn_mixed(desc, batch, q, k_pool, v_pool, o, lse, workspace, workspace_bytes, dev_status, stream);
 

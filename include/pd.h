@@ -237,8 +237,12 @@ PD_API int pd_attn_mixed(const pd_attn_desc *desc, const pd_batch *batch, const 
  * the batch's host-side bounds; rounded to the partition granularity of 8),
  * the decode part on the split-KV kernel over the rest. The call orders both
  * after the work already queued on `stream` and makes `stream` wait for both.
- * Where green contexts cannot be created, or one part is empty, it runs as
- * pd_attn_mixed (or the one part) on `stream`.
+ * Where green contexts cannot be created, one part is empty, or a CUDA tool
+ * is injected into the process (profilers and sanitizers, which may not
+ * follow launches into green contexts; detected from the variables they set in
+ * the environment: CUDA_INJECTION64_PATH or Nsight's injection variables), it
+ * runs as pd_attn_mixed on `stream`; pd_last_kernel() then names
+ * prefill_kernel.
  * Arguments and layouts as pd_attn_mixed; batch->qo_indptr is required; the
  * workspace is that of pd_attn_workspace_size(kind = PD_KIND_MIXED_SPLIT).
  * Host-side state: one pair of green contexts with a stream and two events
