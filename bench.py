@@ -835,6 +835,11 @@ def profile_row(name: str, reps: int) -> None:
         else:
             fn = lambda: pd.pd_kv_append(w["k_new"], w["v_new"], w["k_pool"], w["v_pool"], w["qo_indptr"],
                                          w["kv_len"], w["page_indptr"], w["page_indices"], max_kv_len=512)
+    elif name == "prefill_long":
+        # the bench's compute-bound row: 2 x 8192 causal, 16 heads
+        w = torch_gen.paged_batch(3, [8192] * 2, [8192] * 2, 16, 16, 128, 16)
+        fn = lambda: pd.pd_attn_prefill(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
+                                        w["page_indices"], w["qo_indptr"], max_qo_len=8192, max_kv_len=8192)
     elif name == "prefill_long_small":
         # a reduced compute-bound causal prefill (1 x 4096, 8 heads: 3.4e10 flop
         # over 34 MB, 1024 flop/B), for the tensor-pipe counters of a small capture
@@ -883,7 +888,7 @@ def main():
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile-row", default=None,
-                    help="run only this row's call (decode, decode_mha, append, prefill, prefill_long_small, mixed, mla_decode, pack, "
+                    help="run only this row's call (decode, decode_mha, append, prefill, prefill_long, prefill_long_small, mixed, mla_decode, pack, "
                          "unpack) for ncu")
     ap.add_argument("--profile-reps", type=int, default=3)
     args = ap.parse_args()
