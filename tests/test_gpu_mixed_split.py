@@ -22,7 +22,7 @@ def run_split(case, num_prefill, o_dtype=torch.float32, prefill_sms=0, status=No
     o, lse = pd.pd_attn_mixed_split(d.q, d.k_pool, d.v_pool, d.kv_len, d.page_indptr, d.page_indices,
                                     d.qo_indptr, num_prefill, prefill_sms=prefill_sms, causal=case.causal,
                                     max_qo_len=d.max_qo_len, max_kv_len=d.max_kv_len, o_dtype=o_dtype,
-                                    dev_status=status)
+                                    dev_status=status, layout=case.layout)
     torch.cuda.synchronize()
     return d, o, lse
 
@@ -65,6 +65,23 @@ def test_mixed_split_1p63d_workload_full():
 def test_mixed_split_shapes(qo, kv, hq, hkv, n_pf, sms):
     case = wl.make_attn_case(501 + sum(kv), qo, kv, hq, hkv, 128, 16, wl.BF16, causal=True)
     _, o, lse = run_split(case, n_pf, prefill_sms=sms)
+    check_vs_oracle(case, o, lse)
+
+
+@pytest.mark.parametrize("layout,causal,o_dtype,hq,hkv", [
+    ("NHD", True, torch.bfloat16, 8, 2),      # NHD pools, GQA 4, bf16 output
+    ("HND", False, torch.float32, 4, 4),      # a non-causal prefill part, fp32 output
+    ("HND", True, torch.bfloat16, 32, 8),     # GQA 4 with the prefill tiles packing 4 heads
+])
+def test_mixed_split_layouts_and_outputs(layout, causal, o_dtype, hq, hkv):
+    case = wl.make_attn_case(521 + hq, [640, 129, 1, 1, 1, 1], [700, 129, 900, 17, 2048, 300], hq, hkv, 128, 16,
+                             wl.BF16, causal=causal)
+    if layout == "NHD":
+        case = wl.to_nhd(case)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, o, lse = run_split(case, 2, o_dtype, status=status)
+    assert int(status.item()) == 0
+    assert o.dtype == o_dtype
     check_vs_oracle(case, o, lse)
 
 
