@@ -562,6 +562,27 @@ def measure_rows(args, dev, peaks) -> dict:
                                        "call_pair_TFLOPs": round(flops / (ms * 1e-3) / 1e12, 1), "flops": flops}
     except pd.PdError as e:
         rows["append_then_prefill"] = {"status": str(e)}
+    # the launch floor: 100 calls back to back, no flush between them (the
+    # 84 MB of K and V may stay in L2), one pair of events around them all
+    try:
+        import torch
+        call = lambda: pd.pd_attn_prefill(w["q"], w["k_pool"], w["v_pool"], w["kv_len"], w["page_indptr"],
+                                          w["page_indices"], w["qo_indptr"], max_qo_len=512, max_kv_len=512, o=o)
+        for _ in range(5):
+            call()
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a_ev.record()
+        for _ in range(100):
+            call()
+        b_ev.record()
+        torch.cuda.synchronize()
+        b2b = a_ev.elapsed_time(b_ev) / 100
+        t = flops / (b2b * 1e-3) / 1e12
+        rows["prefill_b2b"] = {"workload": "8 x 512 causal, 40 heads: 100 calls back to back, no flush",
+                               "ms": round(b2b, 5), "TFLOPs": round(t, 1), "frac_bf16": round(t / peaks["bf16"], 4)}
+    except pd.PdError as e:
+        rows["prefill_b2b"] = {"status": str(e)}
     del w
 
     # a compute-bound causal prefill (same kernel): long sequences put the
