@@ -112,3 +112,35 @@ def test_random_mla_batches(seed):
     assert np.array_equal(np.isfinite(lg), fin)
     if fin.any():
         assert float(np.abs(lg[fin] - lse_ref[fin]).max()) <= LSE_TOL
+
+
+@pytest.mark.parametrize("seed", list(range(1100, 1108)))
+def test_random_split_mixed_batches(seed):
+    # pd_attn_mixed_split: 1-3 prefill requests first, then 1-6 decodes, with
+    # a drawn partition size (0: the call's own choice); GQA, page size,
+    # layout and output dtype drawn as above
+    rng = np.random.default_rng(seed)
+    hkv = int(rng.choice([1, 2, 4]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    page = int(rng.choice([8, 16, 32, 64, 128]))
+    n_pf, n_dec = int(rng.integers(1, 4)), int(rng.integers(1, 7))
+    qo = [_length(rng, 1, 300) for _ in range(n_pf)] + [1] * n_dec
+    kv = [q + _length(rng, 0, 400) for q in qo[:n_pf]] + [1 + _length(rng, 0, 2500) for _ in range(n_dec)]
+    case = wl.make_attn_case(seed, qo, kv, hkv * g, hkv, 128, page, wl.BF16, causal=True)
+    if rng.random() < 0.3:
+        case = wl.to_nhd(case)
+    o_dtype = torch.float32 if rng.random() < 0.5 else torch.bfloat16
+    sms = int(rng.choice([0, 8, 16, 24, 48]))
+    d = DevCase(case)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, lse = pd.pd_attn_mixed_split(d.q, d.k_pool, d.v_pool, d.kv_len, d.page_indptr, d.page_indices, d.qo_indptr,
+                                    n_pf, prefill_sms=sms, max_qo_len=d.max_qo_len, max_kv_len=d.max_kv_len,
+                                    o_dtype=o_dtype, layout=case.layout, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    o_ref, lse_ref = oracle.attention_case(case)
+    got = host_f64(o)
+    assert np.isfinite(got).all(), "non-finite output"
+    assert float(np.abs(got - o_ref).max()) <= 1e-2, f"seed {seed}: max |o - oracle| = {np.abs(got - o_ref).max()}"
+    lg = lse.cpu().numpy().astype(np.float64)
+    assert float(np.abs(lg - lse_ref).max()) <= LSE_TOL
