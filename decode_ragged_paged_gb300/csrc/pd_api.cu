@@ -343,6 +343,7 @@ int pd_mla_decode(const pd_mla_desc* desc, const pd_batch* batch, const void* q,
   p.hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
   p.req_info = reinterpret_cast<int4*>(ws + L.req_info);
   p.chunk_list = reinterpret_cast<int2*>(ws + L.chunk_list);
+  p.split_list = reinterpret_cast<int32_t*>(ws + L.split_list);
   p.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   p.part_o = reinterpret_cast<float*>(ws + L.part_o);
   p.status = dev_status;

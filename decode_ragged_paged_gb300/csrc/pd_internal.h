@@ -150,13 +150,14 @@ struct MlaParams {
   int32_t* hdr;
   int4* req_info;
   int2* chunk_list;
+  int32_t* split_list;  // requests cut into several chunks (hdr[2] of them)
   float* part_lse;
   float* part_o;
   int32_t* status;
 };
 
 struct MlaLayout {
-  size_t hdr, req_info, chunk_list, part_lse, part_o, total;
+  size_t hdr, req_info, chunk_list, split_list, part_lse, part_o, total;
   int32_t max_chunks;
 };
 

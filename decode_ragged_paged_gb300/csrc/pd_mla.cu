@@ -187,12 +187,14 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const MlaParams p) {
   __shared__ int s_warp[32];
   __shared__ long long s_total;
   __shared__ int s_carry;
+  __shared__ int s_nsplit;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   pdl_launch_dependents();
   s_bucket[tid] = 0;
   if (tid == 0) {
     s_total = 0;
     s_carry = 0;
+    s_nsplit = 0;
   }
   __syncthreads();
   // 1. validate, total tokens of the valid requests
@@ -303,10 +305,14 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(const MlaParams p) {
       const int pos = atomicAdd(&s_bucket[min((len + kN - 1) / kN, kBuckets - 1)], 1);
       if (pos < p.max_chunks) p.chunk_list[pos] = make_int2(r, c);
     }
+    // the merge kernel's list: requests cut into chunks, in any order
+    if (info.y > 1 && info.z >= 0) p.split_list[atomicAdd(&s_nsplit, 1)] = r;
   }
+  __syncthreads();
   if (tid == 0) {
     p.hdr[0] = min(total, p.max_chunks);
     p.hdr[1] = chunk_len;
+    p.hdr[2] = s_nsplit;
   }
 }
 
@@ -701,42 +707,48 @@ __global__ void __launch_bounds__(kThreadsMla, 1)
 
 // ------------------------------------------------------------------ merge
 // Requests split into chunks: lse2 = log2 sum_c 2^lse2_c, o = sum_c 2^(lse2_c -
-// lse2) o_c. One CTA per (request, pair of heads); a thread owns 4 columns.
+// lse2) o_c. A unit is (request of the plan's split list, pair of heads), a
+// thread owns 4 columns; a small grid strides over the units, so that a batch
+// with few split requests does not launch a CTA per request and head pair.
 __global__ void __launch_bounds__(256) mla_merge_kernel(const MlaParams p) {
   pdl_wait_primary();
-  const int r = blockIdx.x;
-  const int h = blockIdx.y * 2 + (threadIdx.x >> 7);
+  const int hpairs = (p.hq + 1) / 2;
+  const int units = p.hdr[2] * hpairs;
   const int col = (threadIdx.x & 127) * 4;
-  const int4 info = p.req_info[r];
-  if (info.y <= 1 || info.z < 0 || h >= p.hq) return;
-  const float* lse_c = p.part_lse + (int64_t)info.x * p.hq + h;
-  float mx = -INFINITY;
-  for (int c = 0; c < info.y; ++c) mx = fmaxf(mx, lse_c[(int64_t)c * p.hq]);
-  float s = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (mx > -INFINITY) {
-    for (int c = 0; c < info.y; ++c) {
-      const float wgt = exp2f(lse_c[(int64_t)c * p.hq] - mx);
-      const float4 v = *reinterpret_cast<const float4*>(p.part_o + ((int64_t)(info.x + c) * p.hq + h) * kDc + col);
-      s += wgt;
-      acc.x += wgt * v.x;
-      acc.y += wgt * v.y;
-      acc.z += wgt * v.z;
-      acc.w += wgt * v.w;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int r = p.split_list[u / hpairs];
+    const int h = (u % hpairs) * 2 + (threadIdx.x >> 7);
+    const int4 info = p.req_info[r];
+    if (info.y <= 1 || info.z < 0 || h >= p.hq) continue;
+    const float* lse_c = p.part_lse + (int64_t)info.x * p.hq + h;
+    float mx = -INFINITY;
+    for (int c = 0; c < info.y; ++c) mx = fmaxf(mx, lse_c[(int64_t)c * p.hq]);
+    float s = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (mx > -INFINITY) {
+      for (int c = 0; c < info.y; ++c) {
+        const float wgt = exp2f(lse_c[(int64_t)c * p.hq] - mx);
+        const float4 v = *reinterpret_cast<const float4*>(p.part_o + ((int64_t)(info.x + c) * p.hq + h) * kDc + col);
+        s += wgt;
+        acc.x += wgt * v.x;
+        acc.y += wgt * v.y;
+        acc.z += wgt * v.z;
+        acc.w += wgt * v.w;
+      }
     }
+    const float inv = s > 0.f ? 1.0f / s : 0.f;
+    const int64_t o_off = ((int64_t)r * p.hq + h) * kDc + col;
+    if (p.o_dtype == PD_BF16) {
+      uint2 packed;
+      packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.o) + o_off) = packed;
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(p.o) + o_off) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+    if (col == 0 && p.lse != nullptr) p.lse[(int64_t)r * p.hq + h] = s > 0.f ? (mx + log2f(s)) * kLn2 : -INFINITY;
   }
-  const float inv = s > 0.f ? 1.0f / s : 0.f;
-  const int64_t o_off = ((int64_t)r * p.hq + h) * kDc + col;
-  if (p.o_dtype == PD_BF16) {
-    uint2 u;
-    u.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    u.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.o) + o_off) = u;
-  } else {
-    *reinterpret_cast<float4*>(static_cast<float*>(p.o) + o_off) =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  }
-  if (col == 0 && p.lse != nullptr) p.lse[(int64_t)r * p.hq + h] = s > 0.f ? (mx + log2f(s)) * kLn2 : -INFINITY;
 }
 
 // ------------------------------------------------------------------- host
@@ -760,6 +772,8 @@ MlaLayout mla_layout(int32_t batch, int32_t hq) {
   off = align_up(off + sizeof(int4) * (size_t)batch, 256);
   L.chunk_list = off;
   off = align_up(off + sizeof(int2) * (size_t)L.max_chunks, 256);
+  L.split_list = off;
+  off = align_up(off + sizeof(int32_t) * (size_t)(batch > 0 ? batch : 1), 256);
   L.part_lse = off;
   off = align_up(off + sizeof(float) * (size_t)L.max_chunks * hq, 256);
   L.part_o = off;
@@ -805,7 +819,12 @@ int launch_mla(MlaParams& p, const void* q, const void* kv_pool, cudaStream_t st
   profile_end(stream);
   if (e != cudaSuccess) return PD_ERR_CUDA;
   cudaLaunchConfig_t mcfg{};
-  mcfg.gridDim = dim3((unsigned)p.batch, (unsigned)((p.hq + 1) / 2));
+  // two CTAs per SM, or one per unit if the batch has fewer
+  const int64_t merge_units = (int64_t)p.batch * ((p.hq + 1) / 2);
+  int64_t merge_grid = 2 * (int64_t)device_sm_count();
+  if (merge_grid > merge_units) merge_grid = merge_units;
+  if (merge_grid < 1) merge_grid = 1;
+  mcfg.gridDim = dim3((unsigned)merge_grid);
   mcfg.blockDim = dim3(256);
   mcfg.stream = stream;
   mcfg.attrs = attr;
