@@ -51,7 +51,8 @@
 //                          partials, online softmax (lazy O
 //                          rescale), the epilogue (final o and lse, or a fp32
 //                          partial for a request split into chunks);
-//   3. merge   requests split into chunks: log-sum-exp merge of the partials.
+//   3. merge   requests split into chunks (listed by the plan): log-sum-exp
+//              merge of the partials, a small grid striding over them.
 // Every wait is bounded; on a timeout the CTA records PD_DEV_TIMEOUT, drains
 // and frees its TMEM.
 #include <atomic>
