@@ -218,10 +218,52 @@ __global__ void __launch_bounds__(kCopyThreads) kv_append_kernel(const KvCopyPar
 }
 
 // ----------------------------------------------------------------- pack
+// NHD pools: a token's rows of the copied heads are contiguous in the pool, so
+// a unit is (request, layer, K/V, token): one contiguous read of those rows,
+// each row then written to its head's slab of the packed block. Consecutive
+// units are consecutive tokens, so the warps of a CTA read a page's bytes in
+// order (per-head units would read it in 256-byte pieces a token apart).
+__device__ __forceinline__ void pack_nhd_tokens(const KvCopyParams& p, int lane, int64_t warp0, int64_t nwarps) {
+  const int vpr = p.head_dim * p.elem_size / 16;
+  const int64_t units = (int64_t)p.batch * p.layer_count * 2 * p.max_kv_len;
+  for (int64_t u = warp0; u < units; u += nwarps) {
+    const int t = (int)(u % p.max_kv_len);
+    int64_t rest = u / p.max_kv_len;
+    const int kv = (int)(rest % 2);
+    rest /= 2;
+    const int layer = p.layer_begin + (int)(rest % p.layer_count);
+    const int r = (int)(rest / p.layer_count);
+    const int n = __ldg(p.kv_len + r);
+    if (t >= n) continue;
+    const int pa = __ldg(p.page_indptr + r), pb = __ldg(p.page_indptr + r + 1);
+    const int64_t off = __ldg(p.offsets + r);
+    const int64_t block = (int64_t)p.num_layers * 2 * p.head_count * n * vpr * 16;
+    const bool bad_off = (off & 15) != 0 || off < 0 || off + block > p.buf_bytes;
+    if (n > p.max_kv_len || pa < 0 || (int64_t)(pb - pa) * p.page_size < n || bad_off) {
+      if (lane == 0) report(p.status, bad_off ? PD_DEV_BAD_OFFSET : PD_DEV_BAD_PAGE_TABLE);
+      continue;
+    }
+    const int32_t page = __ldg(p.page_indices + pa + t / p.page_size);
+    if (page < 0 || page >= p.num_pages) {
+      if (lane == 0) report(p.status, PD_DEV_BAD_PAGE_TABLE);
+      continue;
+    }
+    const uint8_t* pool = static_cast<const uint8_t*>(kv ? p.src2 : p.src) + (int64_t)layer * p.layer_stride;
+    const uint4* src = reinterpret_cast<const uint4*>(pool) + pool_vec(p, page, p.head_begin, t % p.page_size, vpr);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dst) + off) +
+                 (((int64_t)layer * 2 + kv) * p.head_count * n + t) * vpr;
+    warp_copy_rows(src, vpr, dst, (int64_t)n * vpr, p.head_count, vpr, lane);
+  }
+}
+
 __global__ void __launch_bounds__(kCopyThreads) kv_pack_kernel(const KvCopyParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * kCopyThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kCopyThreads) >> 5;
+  if (p.nhd) {
+    pack_nhd_tokens(p, lane, warp0, nwarps);
+    return;
+  }
   const int kp = (p.max_kv_len + p.page_size - 1) / p.page_size;
   const int64_t units = (int64_t)p.batch * p.layer_count * 2 * p.head_count * kp;
   const int vpr = p.head_dim * p.elem_size / 16;
