@@ -8,10 +8,12 @@
 //   moves as one run; when prefiller and decoder cut pages differently, pages
 //   are split or rebuilt.
 //
-// All three are pure byte moves, bound by HBM bandwidth. Each unit of work is a
-// (page, head) slice, contiguous on both sides for HND pools and a run of
-// head_dim rows hkv rows apart on the pool side for NHD pools; one warp copies
-// it with 16-byte vector loads, several in flight per lane.
+// All three are pure byte moves, bound by HBM bandwidth. A unit of work of
+// pack / unpack is a (page, head) slice, contiguous on both sides for HND pools
+// and a run of head_dim rows hkv rows apart on the pool side for NHD pools
+// (pack from NHD pools takes a token's rows of all copied heads instead, one
+// contiguous run there); one warp copies a unit with 16-byte vector loads,
+// several in flight per lane.
 #include "pd_common.cuh"
 #include "pd_internal.h"
 
@@ -102,8 +104,8 @@ __device__ __forceinline__ int64_t slot_stride_vec(const KvCopyParams& p, int vp
 // range, page k of the request). Page k carries tokens [k*P, min((k+1)*P,
 // kv_len)); packed head h is pool head head_begin + h. For HND pools k is
 // fastest, so consecutive warps touch consecutive bytes of the packed buffer;
-// for NHD pools h is fastest, so consecutive warps cover the rows of one page,
-// which are contiguous in the pool.
+// for NHD pools (unpack) h is fastest, so consecutive warps cover the rows of
+// one page, which are contiguous in the pool.
 struct Unit {
   int r, layer, kv, h, k;
 };
