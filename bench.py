@@ -891,6 +891,13 @@ def profile_row(name: str, reps: int) -> None:
         else:
             fn = lambda: pd.pd_kv_unpack(w["buffer"], w["offsets"], w["k_dst"], w["v_dst"], w["kv_len"],
                                          w["dst_indptr"], w["dst_indices"], max_kv_len=512)
+    elif name in ("pack_nhd", "pack_nhd2"):
+        # the pack from NHD pools (pack_nhd2: 2 of the 40 layers)
+        w = torch_gen.kv_handoff(layers=40 if name == "pack_nhd" else 2)
+        k_nhd = w["k_src"].transpose(2, 3).contiguous()
+        v_nhd = w["v_src"].transpose(2, 3).contiguous()
+        fn = lambda: pd.pd_kv_pack(k_nhd, v_nhd, w["kv_len"], w["src_indptr"], w["src_indices"], w["buffer"],
+                                   w["offsets"], max_kv_len=512, layout="NHD")
     else:
         raise SystemExit(f"unknown row {name}")
     for _ in range(reps):
@@ -910,7 +917,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile-row", default=None,
                     help="run only this row's call (decode, decode_mha, append, prefill, prefill_long, prefill_long_small, mixed, mla_decode, pack, "
-                         "unpack) for ncu")
+                         "unpack, pack_nhd; pack2, unpack2, pack_nhd2: 2 layers) for ncu")
     ap.add_argument("--profile-reps", type=int, default=3)
     args = ap.parse_args()
     if args.profile_row:
