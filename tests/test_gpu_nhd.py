@@ -192,3 +192,24 @@ def test_head_range_pack_from_nhd_pools():
     ref = oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, hc.k_src, hc.v_src,
                          offs, part, head_begin=1, head_count=2, layout=oracle.NHD)
     np.testing.assert_array_equal(buf.cpu().numpy(), ref)
+
+
+def test_layer_range_packs_from_nhd_pools():
+    # layers [0, 1) then [1, 3) of a 3-layer NHD handoff into one buffer equal the
+    # oracle's whole pack; ragged lengths below max_kv_len leave token units idle
+    hc = wl.to_nhd(wl.kv_handoff(seed=411, batch=3, layers=3, heads=5, head_dim=64, src_page=16, dst_page=64,
+                                 dtype=wl.BF16, kv_lens=[77, 16, 130]))
+    L, H, D = hc.num_layers, hc.num_kv_heads, hc.head_dim
+    total = wl.packed_bytes(hc.kv_len, L, H, D, 2)
+    offs = np.zeros(len(hc.kv_len), np.int64)
+    for r in range(1, len(hc.kv_len)):
+        offs[r] = offs[r - 1] + wl.packed_bytes(hc.kv_len[r - 1:r], L, H, D, 2)
+    buf = torch.zeros(total, dtype=torch.uint8, device="cuda")
+    args = (dev_tensor(hc.k_src), dev_tensor(hc.v_src), dev_tensor(hc.kv_len.astype(np.int32)),
+            dev_tensor(hc.src_table.page_indptr), dev_tensor(hc.src_table.page_indices), buf, dev_tensor(offs))
+    pd.pd_kv_pack_layers(*args, 0, 1, max_kv_len=200, layout="NHD")
+    pd.pd_kv_pack_layers(*args, 1, 2, max_kv_len=200, layout="NHD")
+    torch.cuda.synchronize()
+    ref = oracle.kv_pack(hc.kv_len, hc.src_table.page_indptr, hc.src_table.page_indices, hc.k_src, hc.v_src,
+                         offs, total, layout=oracle.NHD)
+    np.testing.assert_array_equal(buf.cpu().numpy(), ref)
